@@ -1,0 +1,379 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Nothing here compares the oracle with itself: each test checks it against a
+hand-worked fixture (tests/golden/), a closed form, a library routine
+(numpy / torch / scipy), brute force, or an independent derivation.
+"""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import bruteforce
+from load_balancing_topk_gb300 import synth
+
+from golden_io import GOLDEN, load, load_hex_pairs
+from plan_checks import check_invariants, derive_dst_pos, group_sizes
+
+
+def _plan_from_fixture(g):
+    R, E, K, S, B = (int(g[k][0]) for k in ("R", "E", "K", "S", "B"))
+    idx = g["topk_idx"].astype(np.int32).reshape(R * S, K)
+    return idx, R, S, K, E, B
+
+
+# --------------------------------------------------------------------------
+# hand-worked fixtures
+@pytest.mark.parametrize("name", ["plan_two_ranks.txt", "plan_three_ranks.txt"])
+def test_plan_matches_hand_worked_fixture(name):
+    g = load(name)
+    idx, R, S, K, E, B = _plan_from_fixture(g)
+    p = oracle.plan(idx, R, S, K, E, B)
+    assert p["status"] == g["status"]
+    np.testing.assert_array_equal(p["counts"], g["counts"])
+    np.testing.assert_array_equal(p["slot_expert"].reshape(-1), g["slot_expert"])
+    np.testing.assert_array_equal(p["slot_lo"].reshape(-1), g["slot_lo"])
+    np.testing.assert_array_equal(p["slot_len"].reshape(-1), g["slot_len"])
+    np.testing.assert_array_equal(p["cu_seqlens"].reshape(-1), g["cu_seqlens"])
+    np.testing.assert_array_equal(p["dst_pos"].reshape(-1), g["dst_pos"])
+    assert oracle.maxvio(p["counts"], R, S, K) == pytest.approx(float(g["maxvio"][0]), abs=0)
+    check_invariants(p, idx, R, S, K, E, B)
+
+
+def test_plan_capacity_fixture():
+    g = load("plan_three_ranks_capacity.txt")
+    idx, R, S, K, E, B = _plan_from_fixture(g)
+    p = oracle.plan(idx, R, S, K, E, B)
+    assert p["status"] == "capacity"
+    np.testing.assert_array_equal(p["counts"], g["counts"])
+    np.testing.assert_array_equal(p["slot_expert"].reshape(-1), g["slot_expert"])
+    np.testing.assert_array_equal(p["cu_seqlens"].reshape(-1), g["cu_seqlens"])
+
+
+@pytest.mark.parametrize("name", ["reduce_grad_small.txt", "reduce_grad_order.txt"])
+def test_reduce_grad_fixture(name):
+    g = load(name)
+    E, R, B, HHp = (int(g[k][0]) for k in ("E", "R", "B", "HHp"))
+    se = g["slot_expert"].astype(np.int32).reshape(R, B)
+    st, h, s = oracle.reduce_grad(se, g["home"].reshape(E, HHp), g["slot"].reshape(R * B, HHp), E)
+    assert st == g["status"]
+    np.testing.assert_array_equal(h.reshape(-1), g["home_out"].astype(np.float32))
+    np.testing.assert_array_equal(s.reshape(-1), g["slot_out"].astype(np.float32))
+
+
+def test_combine_fma_order_fixture():
+    f = {}
+    with open(os.path.join(GOLDEN, "combine_fma_order.txt")) as fh:
+        for line in fh:
+            if line.strip() and not line.startswith("#"):
+                k, *v = line.split()
+                f[k] = v
+    w = np.array([int(x, 16) for x in f["w_bits"]], dtype=np.uint32).view(np.float32).reshape(1, 2)
+    y = np.array([int(x, 16) for x in f["y_bits"]], dtype=np.uint16).reshape(2, 1)
+    dst = np.array([int(x) for x in f["dst_pos"]], dtype=np.int32).reshape(1, 2)
+    out = oracle.combine(y, w, dst)
+    assert out.reshape(-1).tolist() == [int(x, 16) for x in f["out_bits"]]
+
+
+def test_bf16_rounding_fixture():
+    pairs = load_hex_pairs("bf16_rounding.txt")
+    x = np.array([a for a, _ in pairs], dtype=np.uint32).view(np.float32)
+    got = oracle.f32_to_bf16(x)
+    np.testing.assert_array_equal(got, np.array([b for _, b in pairs], dtype=np.uint16))
+
+
+# --------------------------------------------------------------------------
+# library routines
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2**32, size=200000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    # also every tie pattern around a few magnitudes
+    base = rng.integers(0, 2**16, size=4096, dtype=np.uint64).astype(np.uint32) << np.uint32(16)
+    ties = (base | np.uint32(0x8000)).view(np.float32)
+    ties = ties[np.isfinite(ties)]
+    x = np.concatenate([x, ties, rng.standard_normal(10000).astype(np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.f32_to_bf16(x), want)
+
+
+def test_counts_match_bincount():
+    idx, _ = synth.routing(synth.MEDIUM, seed=1, alpha=0.3)
+    np.testing.assert_array_equal(oracle.counts(idx, 64), np.bincount(idx.reshape(-1), minlength=64))
+
+
+def test_R1_is_stable_sort_by_expert():
+    # one rank: nothing is redundant, the static buffer is the assignments sorted by expert
+    # (stable, so token order inside an expert) -- numpy's stable argsort gives it directly.
+    shape = synth.Shape(R=1, E=16, K=3, S=300, H=8, B=2)
+    idx, _ = synth.routing(shape, seed=3, alpha=1.0)
+    p = oracle.plan(idx, 1, 300, 3, 16, 2)
+    assert p["status"] == "ok" and (p["slot_expert"] == -1).all()
+    order = np.argsort(idx.reshape(-1), kind="stable")
+    inv = np.empty_like(order)
+    inv[order] = np.arange(order.size)
+    np.testing.assert_array_equal(p["dst_pos"].reshape(-1), inv)
+
+
+def test_combine_matches_float64_sum_within_one_ulp():
+    shape = synth.Shape(R=2, E=8, K=4, S=50, H=64, B=4)
+    idx, w = synth.routing(shape, seed=5, alpha=0.5)
+    p = oracle.plan(idx, 2, 50, 4, 8, 4)
+    y = synth.bf16_normal(shape.A, shape.H, seed=5, tag=77)
+    out = oracle.combine(y, w, p["dst_pos"])
+    yf = oracle.bf16_to_f32(y).astype(np.float64)
+    ref = np.einsum("tk,tkh->th", w.astype(np.float64), yf[p["dst_pos"]])
+    ref_bf = torch.from_numpy(ref).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.bf16_to_f32(out).astype(np.float64)
+    ulp = np.abs(ref_bf) * 2.0 ** -7 + 1e-30
+    assert (np.abs(got - ref_bf) <= ulp).all()
+    # a wrong index or a dropped term would be far outside one ulp for most entries
+    assert np.mean(got == ref_bf) > 0.95
+
+
+def test_combine_exact_on_dyadic_values():
+    # weights 1/2, 1/4, 1/8, 1/8 and small-integer rows: every partial sum is exact
+    N, K, H = 6, 4, 16
+    dst = np.arange(N * K, dtype=np.int32).reshape(N, K)[:, ::-1].copy()
+    w = np.tile(np.array([0.5, 0.25, 0.125, 0.125], dtype=np.float32), (N, 1))
+    vals = synth.integer_valued((N * K, H), seed=2).astype(np.float32)
+    y = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    out = oracle.bf16_to_f32(oracle.combine(y, w, dst))
+    ref = np.einsum("tk,tkh->th", w, vals[dst])
+    np.testing.assert_array_equal(out, ref.astype(np.float32))
+
+
+def test_reduce_grad_integer_values_exact_against_numpy_sum():
+    E, R, B, HHp = 8, 4, 3, 37
+    se = np.array([[4, 6, -1], [0, 6, 7], [0, -1, -1], [2, 6, 1]], dtype=np.int32)
+    home = synth.integer_valued((E, HHp), seed=1)
+    slot = synth.integer_valued((R * B, HHp), seed=2)
+    st, h, s = oracle.reduce_grad(se, home, slot, E)
+    assert st == "ok"
+    want = home.astype(np.float64).copy()
+    for sidx, e in enumerate(se.reshape(-1)):
+        if e >= 0:
+            want[e] += slot[sidx]
+    np.testing.assert_array_equal(h, want.astype(np.float32))
+    used = se.reshape(-1) >= 0
+    assert (s[used] == 0).all()
+    np.testing.assert_array_equal(s[~used], slot[~used])
+
+
+def test_reduce_grad_single_slot_is_copy_into_zero_home():
+    E, R, B, HHp = 4, 2, 2, 1000
+    se = np.array([[2, -1], [0, 1]], dtype=np.int32)
+    rng = np.random.default_rng(0)
+    slot = rng.standard_normal((R * B, HHp)).astype(np.float32)
+    st, h, s = oracle.reduce_grad(se, np.zeros((E, HHp), np.float32), slot, E)
+    np.testing.assert_array_equal(h[2], slot[0])
+    np.testing.assert_array_equal(h[0], slot[2])
+    np.testing.assert_array_equal(h[1], slot[3])
+    assert (h[3] == 0).all()
+
+
+def test_reduce_grad_order_is_rank_then_slot():
+    # 1 + 2^-24 + 2^-24 depends on order: (1 + 2^-24) + 2^-24 == 1 in fp32,
+    # while 1 + (2^-24 + 2^-24) == 1 + 2^-23. home=1 first, then slots in (r, b) order.
+    E, R, B, HHp = 2, 2, 1, 1
+    se = np.array([[1], [0]], dtype=np.int32)
+    home = np.array([[1.0], [0.0]], dtype=np.float32)
+    slot = np.array([[0.0], [2.0 ** -24]], dtype=np.float32)
+    _, h, _ = oracle.reduce_grad(se, home, slot, E)
+    assert h[0, 0] == np.float32(1.0)
+    se2 = np.array([[0], [0]], dtype=np.int32)
+    slot2 = np.array([[2.0 ** -24], [2.0 ** -24]], dtype=np.float32)
+    _, h2, _ = oracle.reduce_grad(se2, home, slot2, E)
+    assert h2[0, 0] == np.float32(1.0)  # ((1 + u) + u) with u = 2^-24 stays 1 (ties to even)
+    _, h3, _ = oracle.reduce_grad(se2, np.array([[0.0], [0.0]], np.float32), slot2, E)
+    assert h3[0, 0] == np.float32(2.0 ** -23)
+
+
+def test_reduce_grad_rejects_bad_slot_map():
+    se = np.array([[5, -1]], dtype=np.int32)
+    home = np.ones((4, 3), np.float32)
+    slot = np.ones((2, 3), np.float32)
+    st, h, s = oracle.reduce_grad(se, home, slot, 4)
+    assert st == "bad_routing"
+    np.testing.assert_array_equal(h, home)
+    np.testing.assert_array_equal(s, slot)
+
+
+# --------------------------------------------------------------------------
+# closed forms
+def test_maxvio_closed_forms():
+    # perfect balance -> 0; everything on one expert -> E - 1
+    assert oracle.maxvio(np.full(8, 16), R=2, S=32, K=2) == 0.0
+    assert oracle.maxvio(np.array([128, 0, 0, 0, 0, 0, 0, 0]), R=2, S=32, K=2) == 7.0
+    assert oracle.maxvio(np.array([3, 1, 2, 2]), R=2, S=2, K=2) == 0.5
+
+
+def test_round_robin_closed_form():
+    shape = synth.Shape(R=4, E=16, K=3, S=64, H=8, B=4)
+    idx, _ = synth.routing(shape, kind="round_robin")
+    p = oracle.plan(idx, 4, 64, 3, 16, 4)
+    assert p["status"] == "ok"
+    assert oracle.maxvio(p["counts"], 4, 64, 3) == 0.0
+    assert (p["slot_expert"] == -1).all() and p["n_pieces"] == 0
+    width = 4 * 64 * 3 // 16
+    c = group_sizes(p["cu_seqlens"])
+    for r in range(4):
+        want = np.zeros(16 + 4, dtype=np.int64)
+        want[r * 4:(r + 1) * 4] = width
+        np.testing.assert_array_equal(c[r], want)
+
+
+def test_round_trip_k1_unit_weight_is_identity():
+    shape = synth.Shape(R=3, E=6, K=1, S=40, H=24, B=3)
+    idx, _ = synth.routing(shape, seed=2, alpha=2.0)
+    p = oracle.plan(idx, 3, 40, 1, 6, 3)
+    assert p["status"] == "ok"
+    x = synth.hidden(shape, seed=2)
+    buf = oracle.dispatch(x, p["dst_pos"], shape.A)
+    out = oracle.combine(buf, np.ones((shape.N, 1), np.float32), p["dst_pos"])
+    np.testing.assert_array_equal(out, x)
+
+
+def test_round_trip_softmax_weights_within_one_ulp():
+    shape = synth.TINY
+    idx, w = synth.routing(shape, seed=0, alpha=1.0)
+    p = oracle.plan(idx, shape.R, shape.S, shape.K, shape.E, shape.B)
+    x = synth.hidden(shape, seed=0)
+    buf = oracle.dispatch(x, p["dst_pos"], shape.A)
+    # every row of the static buffer is written (rows are hidden rows, in order of dst)
+    flat = p["dst_pos"].reshape(-1)
+    np.testing.assert_array_equal(buf[flat], np.repeat(x, shape.K, axis=0))
+    out = oracle.bf16_to_f32(oracle.combine(buf, w, p["dst_pos"]))
+    xf = oracle.bf16_to_f32(x)
+    assert (np.abs(out - xf) <= np.abs(xf) * 2.0 ** -7).all()
+
+
+# --------------------------------------------------------------------------
+# invariants and the independent lexsort route, over many random tiny cases
+def _random_cases(n):
+    rng = np.random.default_rng(1234)
+    for i in range(n):
+        R = int(rng.integers(1, 5))
+        per = int(rng.integers(1, 4))
+        E = R * per
+        K = int(rng.integers(1, min(E, 3) + 1))
+        S = int(rng.integers(0, 17))
+        B = int(rng.integers(0, 5))
+        alpha = float(rng.uniform(0, 3))
+        placement = "identity" if i % 3 == 0 else "permuted"
+        yield R, E, K, S, B, alpha, placement, i
+
+
+def test_invariants_and_lexsort_on_random_tiny_cases():
+    n_ok = n_cap = 0
+    for R, E, K, S, B, alpha, placement, seed in _random_cases(400):
+        shape = synth.Shape(R=R, E=E, K=K, S=S, H=8, B=B)
+        idx, _ = synth.routing(shape, seed=seed, alpha=alpha, placement=placement)
+        p = oracle.plan(idx, R, S, K, E, B)
+        if p["status"] == "capacity":
+            n_cap += 1
+            # the optimum may or may not fit; home-first needs more than B on some rank
+            continue
+        n_ok += 1
+        check_invariants(p, idx, R, S, K, E, B)
+        d2 = derive_dst_pos(idx, p["cu_seqlens"], p["slot_expert"], p["slot_lo"], R, S, K, E, B)
+        np.testing.assert_array_equal(p["dst_pos"], d2)
+        # the number of pieces is at most #overflowing experts + #deficit ranks - 1
+        c = group_sizes(p["cu_seqlens"])
+        per = E // R
+        keep = np.array([c[e // per, e] for e in range(E)])
+        n_over = int((keep < p["counts"]).sum())
+        loads = np.array([p["counts"][r * per:(r + 1) * per].sum() for r in range(R)])
+        n_def = int((loads < S * K).sum())
+        if p["n_pieces"]:
+            assert p["n_pieces"] <= n_over + n_def - 1
+        # maxvio from the group table equals maxvio from the histogram
+        T2 = keep.copy()
+        for r in range(R):
+            for b in range(B):
+                e = p["slot_expert"][r, b]
+                if e >= 0:
+                    T2[e] += c[r, E + b]
+        assert oracle.maxvio(T2, R, S, K) == oracle.maxvio(p["counts"], R, S, K)
+    assert n_ok > 300 and n_cap > 0
+
+
+def test_config_plans_satisfy_invariants():
+    for name, alpha, kind in [("tiny", 1.0, "zipf"), ("medium", 0.075684, "zipf"),
+                              ("large", 0.195312, "zipf"), ("large", 0.0, "round_robin"),
+                              ("stress", 1.2, "hot")]:
+        s = synth.SHAPES[name]
+        idx, _ = synth.routing(s, seed=0, alpha=alpha, kind=kind)
+        p = oracle.plan(idx, s.R, s.S, s.K, s.E, s.B)
+        check_invariants(p, idx, s.R, s.S, s.K, s.E, s.B)
+        if name != "stress":
+            d2 = derive_dst_pos(idx, p["cu_seqlens"], p["slot_expert"], p["slot_lo"],
+                                s.R, s.S, s.K, s.E, s.B)
+            np.testing.assert_array_equal(p["dst_pos"], d2)
+
+
+# --------------------------------------------------------------------------
+# validation
+def test_validation_rejects_out_of_range_and_duplicates():
+    idx = np.array([[0, 1], [2, 3], [1, 1], [0, 3]], dtype=np.int32)
+    assert oracle.plan(idx, 2, 2, 2, 4, 2)["status"] == "bad_routing"
+    idx = np.array([[0, 1], [2, 4], [1, 2], [0, 3]], dtype=np.int32)
+    assert oracle.plan(idx, 2, 2, 2, 4, 2)["status"] == "bad_routing"
+    idx = np.array([[0, 1], [2, -1], [1, 2], [0, 3]], dtype=np.int32)
+    assert oracle.plan(idx, 2, 2, 2, 4, 2)["status"] == "bad_routing"
+    idx = np.array([[0, 1], [2, 3], [1, 2], [0, 3]], dtype=np.int32)
+    assert oracle.plan(idx, 2, 2, 2, 4, 2)["status"] == "ok"
+
+
+def test_empty_input():
+    p = oracle.plan(np.zeros((0, 2), np.int32), 2, 0, 2, 4, 2)
+    assert p["status"] == "ok"
+    assert (p["cu_seqlens"] == 0).all() and (p["slot_expert"] == -1).all()
+
+
+def test_no_slots_needs_balance():
+    idx, _ = synth.routing(synth.Shape(R=2, E=4, K=2, S=8, H=8, B=0), kind="round_robin")
+    assert oracle.plan(idx, 2, 8, 2, 4, 0)["status"] == "ok"
+    idx = np.zeros((16, 2), np.int32)
+    idx[:, 1] = 1
+    assert oracle.plan(idx, 2, 8, 2, 4, 0)["status"] == "capacity"
+
+
+# --------------------------------------------------------------------------
+# brute force: the home-first plan against the minimum number of replicas
+def test_bruteforce_closed_form_two_ranks():
+    for seed in range(12):
+        shape = synth.Shape(R=2, E=6, K=2, S=6, H=8, B=6)
+        idx, _ = synth.routing(shape, seed=seed, alpha=1.5)
+        T = oracle.counts(idx, 6)
+        assert bruteforce.min_replicas(T, 2, 6, 2, 6) == bruteforce.min_replicas_two_ranks(T, 6, 2)
+
+
+def test_fixture_minimum_replicas():
+    g = load("plan_two_ranks.txt")
+    assert bruteforce.min_replicas(g["counts"], 2, 4, 1, 2) == int(g["min_replicas"][0])
+
+
+def test_home_first_against_optimum_on_tiny_instances():
+    ratios = []
+    for seed in range(6):
+        s = synth.TINY
+        idx, _ = synth.routing(s, seed=seed, alpha=1.0)
+        p = oracle.plan(idx, s.R, s.S, s.K, s.E, s.B)
+        opt = bruteforce.min_replicas(p["counts"], s.R, s.S, s.K, s.B)
+        assert opt is not None and p["n_pieces"] >= opt
+        ratios.append((p["n_pieces"], opt))
+    for seed in range(4):
+        s = synth.Shape(R=3, E=6, K=2, S=8, H=8, B=3)
+        idx, _ = synth.routing(s, seed=seed, alpha=1.5)
+        p = oracle.plan(idx, s.R, s.S, s.K, s.E, s.B)
+        if p["status"] != "ok":
+            continue
+        opt = bruteforce.min_replicas(p["counts"], s.R, s.S, s.K, s.B, max_size=p["n_pieces"])
+        assert opt is not None and p["n_pieces"] >= opt
+        ratios.append((p["n_pieces"], opt))
+    print("home-first pieces vs optimum:", ratios)
