@@ -1,0 +1,189 @@
+/*
+ * mep.h -- C ABI of the GB300 (sm_103a) dynamic-redundant-expert hot path.
+ *
+ * Four steps of one MoE layer, for R "ranks" that are partitions of one
+ * GPU's memory:
+ *   mep_plan        routing histogram + online planner + destination rows
+ *   mep_dispatch    fused permute into the static [R, S*K, H] buffer
+ *   mep_combine     fused weighted unpermute back to [R*S, H]
+ *   mep_reduce_grad redundant-slot gradients folded into home gradients
+ *
+ * Sources (web pages about MoonEP, cited by title and section):
+ *   "月之暗面开源MoonEP：面向MoE训练的专家并行通信库" -- sections
+ *     解决的核心问题 (maxvio), 核心技术 (every rank receives exactly S*K
+ *     tokens; redundant experts planned online from the router output;
+ *     fused permute/unpermute into preset expert-grouped positions of a fixed
+ *     S*K buffer; static shapes remove the per-layer host sync) and
+ *     内存契约与权重布局 (rows [0,E) hold E/R home experts per rank, rows
+ *     [E,E+B) are B prefetch slots; cu_seqlens[E+B]; fp32 gradients with the
+ *     slot rows in a separate reduce buffer viewed as [R,B,H,H']; reduce_grad
+ *     accumulates the slots into the home gradient and zeroes consumed slots).
+ *   "Moonshot AI Open-Sources MoonEP for Expert Parallelism" -- paragraphs
+ *     2 and 3 (maxvio; the S*K invariant; redundant-expert gradients are
+ *     reduced back to their home ranks).
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing, keeps no state between calls and never synchronises
+ *     the host. Work is enqueued on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and runs asynchronously.
+ *   - Tensors are dense, row-major, and must start on a 16-byte boundary.
+ *   - bf16 data is passed as 16-bit bit patterns (mep_bf16).
+ *   - The int return value reports only the checks made on the host before
+ *     anything is enqueued (MEP_ERR_INVALID_ARG) and launch failures
+ *     (MEP_ERR_CUDA). Errors that depend on device data are written to the
+ *     device word `status` (int32, written by mep_plan, read by the others);
+ *     a step that finds *status != 0 on entry does nothing. No kernel traps
+ *     or asserts.
+ */
+#ifndef MEP_H
+#define MEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MEP_API __attribute__((visibility("default")))
+#else
+#define MEP_API
+#endif
+
+typedef uint16_t mep_bf16;
+
+/* Return / status codes. */
+#define MEP_OK 0
+#define MEP_ERR_INVALID_ARG 1   /* host check failed: null pointer, bad size, misalignment */
+#define MEP_ERR_CUDA 2          /* a CUDA launch or attribute call failed */
+#define MEP_ERR_BAD_ROUTING 3   /* device: an expert index out of [0,E) or repeated in a token's row */
+#define MEP_ERR_CAPACITY 4      /* device: some rank needs more than B redundant slots */
+#define MEP_ERR_BAD_POSITION 5  /* device: a dst_pos entry outside [0, R*S*K) */
+#define MEP_ERR_BAD_SLOT_MAP 6  /* device: a slot_expert entry outside [-1, E) */
+#define MEP_ERR_TIMEOUT 7       /* device: a bounded wait inside a kernel gave up */
+
+/* Size limits checked on the host. */
+#define MEP_MAX_E 4096     /* experts */
+#define MEP_MAX_R 1024     /* ranks */
+#define MEP_MAX_K 64       /* experts per token */
+#define MEP_MAX_SLOTS 32768 /* R * B */
+
+/* Library version, (major << 16) | minor. */
+MEP_API int mep_version(void);
+
+/* Human-readable name of a return / status code (static string). */
+MEP_API const char* mep_status_string(int code);
+
+/*
+ * mep_plan_workspace_bytes -- device scratch that mep_plan needs for these
+ * sizes (per-block histograms, planner tables). Writes it to *bytes.
+ * Returns MEP_ERR_INVALID_ARG for sizes mep_plan would reject.
+ */
+MEP_API int mep_plan_workspace_bytes(int R, int S, int K, int E, int B, size_t* bytes);
+
+/*
+ * mep_plan -- routing histogram, online planner and destination rows.
+ *
+ * Problem ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库", 解决的核心问题 and
+ * 核心技术): N = R*S tokens, token t belongs to source rank t / S, and routes
+ * to the K experts topk_idx[t, 0..K-1]. Expert e's home rank is e / (E/R)
+ * (内存契约与权重布局: E/R rows per rank). After planning, every rank
+ * receives exactly S*K (token, expert) assignments.
+ *
+ * Planner (this library's reading of the pages' "online planning"): T_e =
+ * number of assignments to e; each rank keeps, in expert order, at most S*K
+ * of its home experts' tokens (lowest token index first); the remaining
+ * overflow segments, concatenated in expert order, are poured into the
+ * deficits S*K - load_r of under-loaded ranks in rank order; each piece
+ * occupies the rank's next free redundant slot b (0, 1, ...).
+ *
+ * Inputs:
+ *   topk_idx   int32 [R*S, K]   expert ids, each in [0, E), distinct per row
+ *   R, S, K, E, B               ranks, tokens per rank, experts per token,
+ *                               experts (E % R == 0, K <= E), slots per rank
+ *   workspace  device scratch of >= mep_plan_workspace_bytes(...) bytes
+ * Outputs (all written in full on success):
+ *   expert_counts int32 [E]          T_e
+ *   cu_seqlens    int32 [R, E+B]     inclusive running ends of rank r's rows:
+ *                                    row j holds rows [cu[r][j-1], cu[r][j]) of
+ *                                    rank r's buffer (cu[r][-1] := 0); rows
+ *                                    [0,E) are home experts (non-home rows are
+ *                                    empty), rows [E,E+B) redundant slots;
+ *                                    cu[r][E+B-1] == S*K
+ *   slot_expert   int32 [R, B]       expert held by each slot, -1 if unused
+ *   dst_pos       int32 [R*S, K]     row of the static [R*S*K, H] buffer that
+ *                                    assignment (t,k) goes to; a permutation
+ *                                    of [0, R*S*K); inside a group tokens are
+ *                                    in ascending token order
+ *   status        int32 [1]          MEP_OK, MEP_ERR_BAD_ROUTING or
+ *                                    MEP_ERR_CAPACITY (always written)
+ * On MEP_ERR_BAD_ROUTING / MEP_ERR_CAPACITY the device outputs are:
+ * slot_expert all -1, cu_seqlens all 0, dst_pos unspecified; expert_counts
+ * holds T_e for a capacity error and 0 for a routing error.
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG, MEP_ERR_CUDA.
+ */
+MEP_API int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int B,
+             void* workspace, size_t workspace_bytes,
+             int32_t* expert_counts, int32_t* cu_seqlens, int32_t* slot_expert,
+             int32_t* dst_pos, int32_t* status, void* stream);
+
+/*
+ * mep_dispatch -- fused permute ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库",
+ * 核心技术, 零拷贝与静态形状): buf[dst_pos[t,k], :] = hidden[t, :] for every
+ * token t and k, a bit copy into the fixed [R, S*K, H] buffer.
+ *   hidden   bf16 [R*S, H]     H % 8 == 0 (rows are whole 16-byte vectors)
+ *   dst_pos  int32 [R*S, K]    from mep_plan
+ *   status   int32 [1]         read on entry (nonzero: no-op); set to
+ *                              MEP_ERR_BAD_POSITION if an entry is out of
+ *                              range (that row is skipped). May be NULL.
+ *   buf      bf16 [R*S*K, H]   output; must not overlap hidden
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG, MEP_ERR_CUDA.
+ */
+MEP_API int mep_dispatch(const mep_bf16* hidden, const int32_t* dst_pos, int32_t* status,
+                 int R, int S, int K, int H, mep_bf16* buf, void* stream);
+
+/*
+ * mep_combine -- fused weighted unpermute (same section):
+ *   out[t, h] = bf16_rn( sum_{k=0..K-1} topk_w[t,k] * y[dst_pos[t,k], h] )
+ * accumulated in fp32 from 0 with one fused multiply-add per k, in k order,
+ * then rounded to nearest-even bf16.
+ *   y        bf16 [R*S*K, H]   expert outputs in the static buffer layout
+ *                              (may be the dispatch buffer itself)
+ *   topk_w   fp32 [R*S, K]     routing weights, used as given
+ *   dst_pos  int32 [R*S, K]    from mep_plan
+ *   status   int32 [1]         as for mep_dispatch; may be NULL
+ *   out      bf16 [R*S, H]     output; must not overlap y
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG, MEP_ERR_CUDA.
+ */
+MEP_API int mep_combine(const mep_bf16* y, const float* topk_w, const int32_t* dst_pos,
+                int32_t* status, int R, int S, int K, int H, mep_bf16* out,
+                void* stream);
+
+/*
+ * mep_reduce_grad -- fold redundant-slot gradients into home gradients
+ * ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库", 内存契约与权重布局, gradient
+ * paragraph): for every expert e and element i,
+ *   home_grad[e][i] += slot_grad[r][b][i]  over the slots with
+ *                      slot_expert[r][b] == e, in ascending (r, b) order,
+ * then slot_grad[r][b][:] = 0 for every slot with slot_expert[r][b] != -1.
+ * Unused slots (-1) are not touched.
+ *   slot_expert int32 [R, B]          from mep_plan (or any map into [-1, E))
+ *   E, R, B                           sizes
+ *   HHp         int64                 elements per expert matrix (H * H')
+ *   home_grad   fp32 [E, HHp]         in/out
+ *   slot_grad   fp32 [R, B, HHp]      in/out; must not overlap home_grad
+ *   status      int32 [1]             read on entry (nonzero: no-op); set to
+ *                                     MEP_ERR_BAD_SLOT_MAP (nothing changed)
+ *                                     if an entry is outside [-1, E). May be NULL.
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG, MEP_ERR_CUDA.
+ */
+MEP_API int mep_reduce_grad(const int32_t* slot_expert, int E, int R, int B, int64_t HHp,
+                    float* home_grad, float* slot_grad, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEP_H */
