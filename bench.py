@@ -519,7 +519,7 @@ def main():
     nb, times = res["nb"], res["times"]
     K = args.steps
     ms_step = res["total_ms"] / K
-    value = whole_job_gbs(world, res["total_bytes"], res["total_ms"])
+    value = whole_job_gbs(world, K * res["total_bytes"], res["total_ms"])
     med = {k: float(np.median(v)) for k, v in times.items()}
     avg = {k: float(np.mean(v)) for k, v in times.items()}
     peak, peak_kind = measured_peak()
