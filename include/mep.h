@@ -130,6 +130,36 @@ MEP_API int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int B,
              int32_t* dst_pos, int32_t* status, void* stream);
 
 /*
+ * mep_plan_static_scratch -- mep_plan without a caller-supplied workspace.
+ * (The pages have no counterpart: this is an allocation-free variant of the
+ * same planner for callers that cannot allocate device memory, such as a
+ * host program that reaches the GPU only through this ABI, or a runtime whose
+ * device memory belongs to one pool allocator that every allocation must go
+ * through.)
+ *
+ * Arguments, outputs, status values and errors are those of mep_plan. The
+ * scratch is a fixed array of MEP_PLAN_STATIC_SCRATCH_BYTES compiled into the
+ * library; every GPU that loads the library keeps it until the process exits.
+ *   - Sizes whose mep_plan_workspace_bytes exceeds
+ *     MEP_PLAN_STATIC_SCRATCH_BYTES are rejected with MEP_ERR_INVALID_ARG
+ *     before anything is enqueued.
+ *   - No cudaMalloc, cudaFree or allocating library call is made.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture. MEP_ERR_CUDA if the lookup fails.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents (each call writes every scratch byte it later reads, so no
+ *     clearing is needed). Calls that overlap on the GPU -- on different
+ *     streams, or from several host threads without ordering -- race on it:
+ *     order them on one stream.
+ */
+#define MEP_PLAN_STATIC_SCRATCH_BYTES (4u << 20) /* 4 MiB per device */
+MEP_API int mep_plan_static_scratch(const int32_t* topk_idx, int R, int S, int K, int E, int B,
+                                    int32_t* expert_counts, int32_t* cu_seqlens,
+                                    int32_t* slot_expert, int32_t* dst_pos, int32_t* status,
+                                    void* stream);
+
+/*
  * mep_dispatch -- fused permute ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库",
  * 核心技术, 零拷贝与静态形状): buf[dst_pos[t,k], :] = hidden[t, :] for every
  * token t and k, a bit copy into the fixed [R, S*K, H] buffer.

@@ -57,6 +57,7 @@ SIGNATURES = [
     ("mep_status_string", ctypes.c_char_p, [_I]),
     ("mep_plan_workspace_bytes", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     ("mep_plan", _I, [_VP, _I, _I, _I, _I, _I, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]),
+    ("mep_plan_static_scratch", _I, [_VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("mep_dispatch", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
     ("mep_combine", _I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
     ("mep_reduce_grad", _I, [_VP, _I, _I, _I, ctypes.c_int64, _VP, _VP, _VP, _VP]),
