@@ -148,6 +148,33 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with
+// launch_pdl() may start while its predecessor in the stream is finishing;
+// it must call pdl_wait() before touching anything the predecessor writes.
+// pdl_launch_dependents() lets the next kernel in the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // host helpers (defined in abi.cu)
 int sm_count();                                     // SMs of the current device
 int set_max_dynamic_smem(const void* func, int bytes);  // cudaFuncSetAttribute, cached

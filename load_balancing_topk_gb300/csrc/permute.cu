@@ -29,11 +29,11 @@
 #ifndef MEP_DISPATCH_CHUNK
 #define MEP_DISPATCH_CHUNK 16384
 #endif
-#ifndef MEP_DISPATCH_CTAS_PER_SM
-#define MEP_DISPATCH_CTAS_PER_SM 1
+#ifndef MEP_DISPATCH_MAX_CTAS_PER_SM
+#define MEP_DISPATCH_MAX_CTAS_PER_SM 2
 #endif
 #ifndef MEP_COMBINE_WARPS
-#define MEP_COMBINE_WARPS 8
+#define MEP_COMBINE_WARPS 4
 #endif
 
 namespace mep {
@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(32)
     k_dispatch(const uint8_t* __restrict__ hidden, const int32_t* __restrict__ dst_pos,
                int32_t* status, long long N, int K, long long row_bytes, int chunk_bytes,
                int nchunk, long long nrows, uint8_t* __restrict__ buf) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (read_status(status) != 0) return;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * chunk_bytes);
@@ -176,6 +178,8 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
     k_combine(const uint4* __restrict__ y, const float* __restrict__ topk_w,
               const int32_t* __restrict__ dst_pos, int32_t* status, long long N, int Kr,
               long long vpr, long long nrows, uint4* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (read_status(status) != 0) return;
   const int K = KT > 0 ? KT : Kr;
   const int lane = threadIdx.x & 31;
@@ -241,8 +245,8 @@ cudaError_t launch_combine(const uint4* y, const float* w, const int32_t* dst, i
   const long long want = (N + MEP_COMBINE_WARPS - 1) / MEP_COMBINE_WARPS;
   const long long cap = (long long)sm_count() * 64;
   const int grid = int(want < cap ? want : cap);
-  k_combine<KT><<<grid, 32 * MEP_COMBINE_WARPS, 0, st>>>(y, w, dst, status, N, K, vpr, nrows, out);
-  return cudaGetLastError();
+  return launch_pdl(k_combine<KT>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0, st, y, w, dst,
+                    status, N, K, vpr, nrows, out);
 }
 
 }  // namespace
@@ -272,12 +276,16 @@ extern "C" int mep_dispatch(const mep_bf16* hidden, const int32_t* dst_pos, int3
   const int smem = kStages * chunk + kStages * 8;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_dispatch), smem)) return MEP_ERR_CUDA;
   const long long units = N * nchunk;
-  const long long cap = (long long)sm_count() * MEP_DISPATCH_CTAS_PER_SM;
+  // as many rings per SM as fit its shared memory, up to the cap
+  int per_sm = (220 * 1024) / smem;
+  per_sm = per_sm < 1 ? 1 : (per_sm > MEP_DISPATCH_MAX_CTAS_PER_SM ? MEP_DISPATCH_MAX_CTAS_PER_SM : per_sm);
+  const long long cap = (long long)sm_count() * per_sm;
   const int grid = int(units < cap ? units : cap);
-  k_dispatch<<<grid, 32, smem, static_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const uint8_t*>(hidden), dst_pos, status, N, K, row_bytes, chunk, nchunk,
-      N * K, reinterpret_cast<uint8_t*>(buf));
-  return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
+  const cudaError_t err =
+      launch_pdl(k_dispatch, dim3(grid), dim3(32), smem, static_cast<cudaStream_t>(stream),
+                 reinterpret_cast<const uint8_t*>(hidden), dst_pos, status, N, K, row_bytes,
+                 chunk, nchunk, N * K, reinterpret_cast<uint8_t*>(buf));
+  return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
 
 extern "C" int mep_combine(const mep_bf16* y, const float* topk_w, const int32_t* dst_pos,

@@ -6,15 +6,19 @@
 // 内存契约与权重布局 (E/R home rows per rank, B slot rows, cu_seqlens[E+B]).
 // maxvio and T_e: same page, section 解决的核心问题.
 //
-// Three launches, all asynchronous on the caller's stream:
-//   k_hist     grid over tiles of assignments: per-tile expert counts
-//              (warp-aggregated with __match_any_sync) and routing checks.
-//   k_plan     one CTA: tile counts -> T_e and per-tile exclusive prefixes,
-//              home-first keep, overflow pour into deficits, slot table,
-//              cu_seqlens, and the per-expert row bases used by k_offsets.
+// Three launches, all asynchronous on the caller's stream; the second and
+// third use programmatic dependent launch, so each starts while its
+// predecessor drains and waits (griddepcontrol.wait) only before reading it:
+//   k_hist     grid over tiles of <= 2048 assignments: per-tile expert counts
+//              (shared-memory atomics) and routing checks, one token per
+//              thread.
+//   k_plan     one CTA: tile counts -> T_e and per-tile exclusive prefixes
+//              (16-byte column loads), home-first keep, overflow pour into
+//              deficits, slot table, cu_seqlens, per-expert row bases.
 //   k_offsets  grid over the same tiles: each assignment's index in its
 //              expert's token-ordered list (tile prefix + warp prefix + rank
-//              inside the warp), mapped to its destination row.
+//              inside the warp from __match_any_sync), mapped to its
+//              destination row.
 // The planner's rule is home-first: a rank keeps, in expert order, at most
 // S*K of its home experts' tokens; the overflow segments, in expert order,
 // fill the under-loaded ranks' deficits in rank order, one slot per piece.
@@ -28,11 +32,12 @@ namespace {
 
 constexpr int kTileThreads = 256;            // k_hist / k_offsets block size (8 warps)
 constexpr int kTileWarps = kTileThreads / 32;
-constexpr int kTileAssign = 4096;            // assignments per tile (upper bound)
-constexpr int kWarpIters = kTileAssign / (32 * kTileWarps);  // 16 iterations per warp
+constexpr int kTileAssign = 2048;            // assignments per tile (upper bound)
+constexpr int kWarpIters = kTileAssign / (32 * kTileWarps);  // 8 iterations per warp
 constexpr int kPlanThreads = 1024;           // k_plan block size
+constexpr int kMaxScanGroups = 64;           // tile groups in k_plan's prefix pass
 
-// tokens per tile: as many as fit 4096 assignments, a multiple of 4 so that
+// tokens per tile: as many as fit 2048 assignments, a multiple of 4 so that
 // every tile starts on a 16-byte boundary of topk_idx.
 inline int tile_tokens(int K) { return (kTileAssign / K) & ~3; }
 
@@ -45,14 +50,11 @@ struct PlanWs {
   int* pc_count;     // [E]
   int* piece_lo;     // [E+R] first list index covered by the piece
   int* piece_base;   // [E+R] global row of the piece's first token
-  int* piece_expert; // [E+R]
-  int* slot_lo;      // [R*B]
-  int* slot_len;     // [R*B]
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-size_t carve(PlanWs* ws, char* base, int nblk, int R, int E, int B) {
+size_t carve(PlanWs* ws, char* base, int nblk, int R, int E) {
   size_t off = 0;
   auto take = [&](int** p, size_t n) {
     if (ws) *p = reinterpret_cast<int*>(base + off);
@@ -68,57 +70,63 @@ size_t carve(PlanWs* ws, char* base, int nblk, int R, int E, int B) {
   take(&w->pc_count, E);
   take(&w->piece_lo, size_t(E) + R);
   take(&w->piece_base, size_t(E) + R);
-  take(&w->piece_expert, size_t(E) + R);
-  take(&w->slot_lo, size_t(R) * (B > 0 ? B : 1));
-  take(&w->slot_len, size_t(R) * (B > 0 ? B : 1));
   return off;
 }
 
-// Stage one tile of topk_idx into shared memory (16-byte loads; the tile
-// start is 16-byte aligned, the tail is loaded element by element).
-__device__ __forceinline__ void stage_tile(const int32_t* __restrict__ g, int na, int* s_idx) {
-  const int nv = na >> 2;
-  const int4* g4 = reinterpret_cast<const int4*>(g);
-  int4* s4 = reinterpret_cast<int4*>(s_idx);
-  for (int i = threadIdx.x; i < nv; i += blockDim.x) s4[i] = __ldg(g4 + i);
-  for (int i = (nv << 2) + threadIdx.x; i < na; i += blockDim.x) s_idx[i] = __ldg(g + i);
-}
-
 // ---------------------------------------------------------------------------
-// k_hist: tile counts and routing checks.
+// k_hist: tile counts and routing checks. Thread tt owns token t0 + tt (and
+// t0 + tt + 256, ...): it loads the token's K expert ids, checks each is in
+// [0, E) and differs from the earlier ones, and counts them.
 __global__ void __launch_bounds__(kTileThreads)
     k_hist(const int32_t* __restrict__ topk_idx, int N, int K, int E, int tok_per_tile,
            PlanWs ws) {
-  extern __shared__ int smem[];
-  int* s_idx = smem;                 // [kTileAssign]
-  int* s_cnt = smem + kTileAssign;   // [E]
+  pdl_launch_dependents();
+  extern __shared__ int s_cnt[];  // [E]
   __shared__ int s_err;
   const int blk = blockIdx.x;
   const int t0 = blk * tok_per_tile;
   const int ntok = min(tok_per_tile, N - t0);
-  const int na = ntok * K;
   if (threadIdx.x == 0) s_err = 0;
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
-  stage_tile(topk_idx + size_t(t0) * K, na, s_idx);
   __syncthreads();
 
-  const int lane = threadIdx.x & 31;
   bool bad = false;
-  for (int a0 = 0; a0 < na; a0 += blockDim.x) {
-    const int a = a0 + threadIdx.x;
-    const bool in = a < na;
-    int e = in ? s_idx[a] : -1;
-    bool ok = in && e >= 0 && e < E;
-    if (ok) {
-      const int t = a / K, k = a - t * K;
-      for (int k2 = 0; k2 < k; ++k2)
-        if (s_idx[t * K + k2] == e) ok = false;
-    }
-    if (in && !ok) bad = true;
-    const unsigned m = __ballot_sync(MEP_FULL_MASK, ok);
-    if (ok) {
-      const unsigned peers = __match_any_sync(m, e);
-      if (lane == __ffs(peers) - 1) atomicAdd(&s_cnt[e], __popc(peers));
+  for (int tt = threadIdx.x; tt < ntok; tt += blockDim.x) {
+    const int32_t* row = topk_idx + (size_t(t0) + tt) * K;
+    if (K <= 8) {
+      int v[8];
+      if ((K & 3) == 0) {  // rows start on 16-byte boundaries
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (4 * q < K) {
+            const int4 x = __ldg(reinterpret_cast<const int4*>(row) + q);
+            v[4 * q] = x.x;
+            v[4 * q + 1] = x.y;
+            v[4 * q + 2] = x.z;
+            v[4 * q + 3] = x.w;
+          }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < K) v[k] = __ldg(row + k);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k >= K) break;
+        bool ok = v[k] >= 0 && v[k] < E;
+#pragma unroll
+        for (int k2 = 0; k2 < k; ++k2) ok = ok && (v[k2] != v[k]);
+        if (ok) atomicAdd(&s_cnt[v[k]], 1);
+        else bad = true;
+      }
+    } else {
+      for (int k = 0; k < K; ++k) {
+        const int e = __ldg(row + k);
+        bool ok = e >= 0 && e < E;
+        for (int k2 = 0; k2 < k && ok; ++k2) ok = __ldg(row + k2) != e;
+        if (ok) atomicAdd(&s_cnt[e], 1);
+        else bad = true;
+      }
     }
   }
   if (bad) s_err = MEP_ERR_BAD_ROUTING;
@@ -148,7 +156,97 @@ __device__ void plan_fail(const PlanArgs& a, int code, bool zero_counts) {
   if (threadIdx.x == 0) *a.status = code;
 }
 
+template <int W> struct Vec;
+template <> struct Vec<1> {
+  using T = int;
+  static __device__ __forceinline__ int get(const int& v, int) { return v; }
+  static __device__ __forceinline__ int make(const int* s) { return s[0]; }
+};
+template <> struct Vec<4> {
+  using T = int4;
+  static __device__ __forceinline__ int get(const int4& v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+  }
+  static __device__ __forceinline__ int4 make(const int* s) {
+    return make_int4(s[0], s[1], s[2], s[3]);
+  }
+};
+
+// T_e and the per-tile exclusive prefixes of the tile counts, in place.
+// Columns are W experts wide; thread (g, c) owns tiles [g*tpg, (g+1)*tpg)
+// of column c.
+template <int W>
+__device__ void tile_prefix(const PlanArgs& a, int* sPart, int* sT) {
+  using V = typename Vec<W>::T;
+  const int E = a.E, nblk = a.nblk, nthr = blockDim.x, tid = threadIdx.x;
+  const int nc = E / W;
+  const int Gs = nc >= nthr ? 1 : min(kMaxScanGroups, nthr / nc);
+  const int tpg = (nblk + Gs - 1) / Gs;
+  V* h = reinterpret_cast<V*>(a.ws.blockhist);
+  for (int x = tid; x < Gs * nc; x += nthr) {
+    const int g = x / nc, c = x - g * nc;
+    const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
+    int s[W];
+#pragma unroll
+    for (int j = 0; j < W; ++j) s[j] = 0;
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) {
+      const V v = h[size_t(b) * nc + c];
+#pragma unroll
+      for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
+    }
+#pragma unroll
+    for (int j = 0; j < W; ++j) sPart[g * E + c * W + j] = s[j];
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += nthr) {
+    int run = 0;
+    for (int g = 0; g < Gs; ++g) {
+      const int v = sPart[g * E + e];
+      sPart[g * E + e] = run;
+      run += v;
+    }
+    sT[e] = run;
+    a.counts[e] = run;
+  }
+  __syncthreads();
+  for (int x = tid; x < Gs * nc; x += nthr) {
+    const int g = x / nc, c = x - g * nc;
+    const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
+    int run[W];
+#pragma unroll
+    for (int j = 0; j < W; ++j) run[j] = sPart[g * E + c * W + j];
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) {
+      const V v = h[size_t(b) * nc + c];
+      h[size_t(b) * nc + c] = Vec<W>::make(run);
+#pragma unroll
+      for (int j = 0; j < W; ++j) run[j] += Vec<W>::get(v, j);
+    }
+  }
+}
+
+// Exclusive scan of a short array by warp 0 (out may alias in; out[n] =
+// total). Ends with __syncthreads().
+__device__ void warp0_excl_scan(const int* in, int* out, int n) {
+  if ((threadIdx.x >> 5) == 0) {
+    const int lane = threadIdx.x & 31;
+    int carry = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      const int i = i0 + lane;
+      const int v = i < n ? in[i] : 0;
+      const int incl = warp_incl_scan(v);
+      if (i < n) out[i] = carry + incl - v;
+      carry += __shfl_sync(MEP_FULL_MASK, incl, 31);
+    }
+    if (lane == 0) out[n] = carry;
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
+  pdl_wait();                // k_hist's counts and error words
+  pdl_launch_dependents();
   extern __shared__ int smem[];
   const int E = a.E, R = a.R, B = a.B, nblk = a.nblk;
   const int per = E / R;
@@ -157,23 +255,25 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
   const int EP = E + 1, RP = R + 1;
-  const int npart = max(nthr, E);
+  const int npart = max(4 * nthr, E);
   int* sT = smem;                // [E+1]
   int* sPre = sT + EP;           // [E+1]
-  int* sKeep = sPre + EP;        // [E]
-  int* sOv = sKeep + E;          // [E+1]
+  int* sKeep = sPre + EP;        // [E+1]
+  int* sOv = sKeep + EP;         // [E+1]
   int* sOst = sOv + EP;          // [E+1]
-  int* sOlist = sOst + EP;       // [E]
-  int* sPcBeg = sOlist + E;      // [E]
-  int* sPcCnt = sPcBeg + E;      // [E]
-  int* sPart = sPcCnt + E;       // [max(nthr, E)]
-  int* sLoad = sPart + npart;    // [R+1]
-  int* sDef = sLoad + RP;        // [R+1]
+  int* sOlist = sOst + EP;       // [E+1]
+  int* sFlag = sOlist + EP;      // [E+1] overflow flags, then their numbering
+  int* sPcBeg = sFlag + EP;      // [E+1]
+  int* sPcCnt = sPcBeg + EP;     // [E+1]
+  int* sPlen = sPcCnt + EP;      // [E+R] piece lengths, by global piece index
+  int* sPart = sPlen + E + R;    // [max(4*nthr, E)]
+  int* sDef = sPart + npart;     // [R+1]
   int* sDst = sDef + RP;         // [R+1]
   int* sNp = sDst + RP;          // [R+1]
   int* sPex = sNp + RP;          // [R+1]
+  int* sQ0 = sPex + RP;          // [R+1] first overflow segment of each rank
   __shared__ int s_warp[33];
-  __shared__ int s_errblk, s_cap, s_nov;
+  __shared__ int s_errblk, s_cap;
 
   // 0. routing errors found by k_hist (lowest tile wins)
   if (tid == 0) {
@@ -189,79 +289,44 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     return;
   }
 
-  // 1. T_e and exclusive prefixes over tiles, in place. Thread (g, e) owns
-  //    tiles [g*nblk/Gs, (g+1)*nblk/Gs) of expert e.
-  const int Gs = (E >= nthr) ? 1 : nthr / E;
-  for (int x = tid; x < Gs * E; x += nthr) {
-    const int g = x / E, e = x - g * E;
-    const int b0 = int((long long)g * nblk / Gs), b1 = int((long long)(g + 1) * nblk / Gs);
-    const int* h = a.ws.blockhist + e;
-    int s = 0;
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) s += h[size_t(b) * E];
-    sPart[x] = s;
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += nthr) {
-    int run = 0;
-    for (int g = 0; g < Gs; ++g) {
-      const int v = sPart[g * E + e];
-      sPart[g * E + e] = run;
-      run += v;
-    }
-    sT[e] = run;
-    a.counts[e] = run;
-  }
-  __syncthreads();
-  for (int x = tid; x < Gs * E; x += nthr) {
-    const int g = x / E, e = x - g * E;
-    const int b0 = int((long long)g * nblk / Gs), b1 = int((long long)(g + 1) * nblk / Gs);
-    int* h = a.ws.blockhist + e;
-    int run = sPart[x];
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) {
-      const int v = h[size_t(b) * E];
-      h[size_t(b) * E] = run;
-      run += v;
-    }
-  }
+  // 1. T_e and per-tile exclusive prefixes
+  if ((E & 3) == 0) tile_prefix<4>(a, sPart, sT);
+  else tile_prefix<1>(a, sPart, sT);
 
-  // 2. home loads and home-first keep
+  // 2. home-first keep: the count of e's earlier home experts is a
+  //    difference of the running sum of T
   block_excl_scan(sT, sPre, E, s_warp, true);
   for (int e = tid; e < E; e += nthr) {
     const int r = e / per;
-    const int before = sPre[e] - sPre[r * per];   // earlier home experts of r
+    const int before = sPre[e] - sPre[r * per];
     const int kp = max(0, min(sT[e], SK - before));
     sKeep[e] = kp;
     sOv[e] = sT[e] - kp;
+    sFlag[e] = sOv[e] > 0 ? 1 : 0;
     a.ws.keep[e] = kp;
   }
-  for (int r = tid; r < R; r += nthr) {
-    const int load = sPre[(r + 1) * per] - sPre[r * per];
-    sLoad[r] = load;
-    sDef[r] = max(0, SK - load);
-  }
+  for (int r = tid; r < R; r += nthr)
+    sDef[r] = max(0, SK - (sPre[(r + 1) * per] - sPre[r * per]));
   __syncthreads();
 
   // 3. overflow segments (expert order) and deficits (rank order) on one line
   block_excl_scan(sOv, sOst, E, s_warp, true);
-  for (int e = tid; e < E; e += nthr) sPre[e] = sOv[e] > 0 ? 1 : 0;
-  __syncthreads();
-  block_excl_scan(sPre, sPre, E, s_warp, true);
+  block_excl_scan(sFlag, sFlag, E, s_warp, true);
   for (int e = tid; e < E; e += nthr)
-    if (sOv[e] > 0) sOlist[sPre[e]] = e;
-  if (tid == 0) s_nov = sPre[E];
-  block_excl_scan(sDef, sDst, R, s_warp, true);
+    if (sOv[e] > 0) sOlist[sFlag[e]] = e;
+  warp0_excl_scan(sDef, sDst, R);
+  const int nov = sFlag[E];
 
   // 4. pieces of each under-loaded rank: the overflow segments that meet
-  //    [Dst_r, Dst_r + d_r), in expert order, one slot each.
-  const int nov = s_nov;
+  //    [Dst_r, Dst_r + d_r), in expert order, one slot each. First count
+  //    them (and find the first segment), then number them globally in rank
+  //    order, then write them.
   for (int r = tid; r < R; r += nthr) {
-    int np = 0;
+    int np = 0, q0 = 0;
     const int d = sDef[r];
     if (d > 0) {
       const int lo = sDst[r], hi = lo + d;
-      int q0 = 0, q1 = nov;  // first q whose segment ends after lo
+      int q1 = nov;  // first q whose segment ends after lo
       while (q0 < q1) {
         const int m = (q0 + q1) >> 1;
         const int e = sOlist[m];
@@ -270,49 +335,42 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
       for (int q = q0; q < nov; ++q) {
         const int e = sOlist[q];
         const int os = sOst[e], oe = os + sOv[e];
-        const int s = max(os, lo), en = min(oe, hi);
-        if (s >= en) break;
-        if (np >= B) {
-          s_cap = 1;
-          break;
-        }
-        a.slot_expert[r * B + np] = e;
-        a.ws.slot_lo[r * B + np] = sKeep[e] + (s - os);
-        a.ws.slot_len[r * B + np] = en - s;
+        if (max(os, lo) >= min(oe, hi)) break;
         ++np;
-        if (en < oe) break;
+        if (min(oe, hi) < oe) break;
       }
     }
-    for (int b = np; b < B; ++b) {
-      a.slot_expert[r * B + b] = -1;
-      a.ws.slot_lo[r * B + b] = 0;
-      a.ws.slot_len[r * B + b] = 0;
-    }
+    if (np > B) s_cap = 1;
     sNp[r] = np;
+    sQ0[r] = q0;
   }
   __syncthreads();
   if (s_cap) {
     plan_fail(a, MEP_ERR_CAPACITY, false);
     return;
   }
-
-  // 5. global piece numbering: rank order (= expert order along the line)
-  block_excl_scan(sNp, sPex, R, s_warp, true);
+  warp0_excl_scan(sNp, sPex, R);
   for (int e = tid; e < E; e += nthr) {
     sPcBeg[e] = INT_MAX;
     sPcCnt[e] = 0;
   }
   __syncthreads();
   for (int r = tid; r < R; r += nthr) {
-    for (int b = 0; b < sNp[r]; ++b) {
+    const int np = sNp[r];
+    const int lo = sDst[r], hi = lo + sDef[r];
+    for (int b = 0; b < np; ++b) {
+      const int e = sOlist[sQ0[r] + b];
+      const int os = sOst[e], oe = os + sOv[e];
+      const int s = max(os, lo), en = min(oe, hi);
       const int g = sPex[r] + b;
       if (g >= E + R) break;  // cannot happen: pieces <= overflow experts + deficit ranks - 1
-      const int e = a.slot_expert[r * B + b];
-      a.ws.piece_lo[g] = a.ws.slot_lo[r * B + b];
-      a.ws.piece_expert[g] = e;
+      a.slot_expert[r * B + b] = e;
+      a.ws.piece_lo[g] = sKeep[e] + (s - os);
+      sPlen[g] = en - s;
       atomicMin(&sPcBeg[e], g);
       atomicAdd(&sPcCnt[e], 1);
     }
+    for (int b = np; b < B; ++b) a.slot_expert[r * B + b] = -1;
   }
   __syncthreads();
   for (int e = tid; e < E; e += nthr) {
@@ -320,16 +378,16 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     a.ws.pc_count[e] = sPcCnt[e];
   }
 
-  // 6. cu_seqlens, one warp per rank; also the global first row of every
+  // 5. cu_seqlens, one warp per rank; also the global first row of every
   //    home row and piece.
   for (int r = warp; r < R; r += nwarps) {
     int carry = 0;
-    const int np = sNp[r];
+    const int np = sNp[r], pex = sPex[r];
     for (int j0 = 0; j0 < G; j0 += 32) {
       const int j = j0 + lane;
       int c = 0;
       if (j < E) c = (j / per == r) ? sKeep[j] : 0;
-      else if (j < G) c = a.ws.slot_len[r * B + (j - E)];
+      else if (j - E < np) c = sPlen[pex + (j - E)];
       const int incl = warp_incl_scan(c);
       if (j < G) {
         a.cu[size_t(r) * G + j] = carry + incl;
@@ -337,7 +395,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
         if (j < E) {
           if (j / per == r) a.ws.home_base[j] = start;
         } else if (j - E < np) {
-          a.ws.piece_base[sPex[r] + (j - E)] = start;
+          a.ws.piece_base[pex + (j - E)] = start;
         }
       }
       carry += __shfl_sync(MEP_FULL_MASK, incl, 31);
@@ -351,7 +409,6 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
 __global__ void __launch_bounds__(kTileThreads)
     k_offsets(const int32_t* __restrict__ topk_idx, int N, int K, int E, int tok_per_tile,
               PlanWs ws, const int32_t* __restrict__ status, int32_t* __restrict__ dst_pos) {
-  if (read_status(status) != 0) return;
   extern __shared__ int smem[];
   int* s_idx = smem;                    // [kTileAssign]
   int* s_wcnt = smem + kTileAssign;     // [kTileWarps, E]
@@ -360,8 +417,19 @@ __global__ void __launch_bounds__(kTileThreads)
   const int ntok = min(tok_per_tile, N - t0);
   const int na = ntok * K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // the tile's routing does not depend on the planner: stage it first
+  {
+    const int32_t* g = topk_idx + size_t(t0) * K;
+    const int nv = na >> 2;
+    const int4* g4 = reinterpret_cast<const int4*>(g);
+    int4* s4 = reinterpret_cast<int4*>(s_idx);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) s4[i] = __ldg(g4 + i);
+    for (int i = (nv << 2) + threadIdx.x; i < na; i += blockDim.x) s_idx[i] = __ldg(g + i);
+  }
   for (int i = threadIdx.x; i < kTileWarps * E; i += blockDim.x) s_wcnt[i] = 0;
-  stage_tile(topk_idx + size_t(t0) * K, na, s_idx);
+  pdl_wait();                           // the planner's tables and status
+  pdl_launch_dependents();
+  if (read_status(status) != 0) return;
   __syncthreads();
 
   // Warp w owns the contiguous assignment range [wbeg, wend) of the tile,
@@ -450,7 +518,7 @@ extern "C" int mep_plan_workspace_bytes(int R, int S, int K, int E, int B, size_
   if (bytes == nullptr) return MEP_ERR_INVALID_ARG;
   const int rc = plan_check(R, S, K, E, B);
   if (rc != MEP_OK) return rc;
-  *bytes = carve(nullptr, nullptr, plan_nblk(R, S, K), R, E, B);
+  *bytes = carve(nullptr, nullptr, plan_nblk(R, S, K), R, E);
   return MEP_OK;
 }
 
@@ -467,17 +535,17 @@ extern "C" int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int
       (N > 0 && (topk_idx == nullptr || dst_pos == nullptr)))
     return MEP_ERR_INVALID_ARG;
   if (!aligned16(workspace) || (topk_idx && !aligned16(topk_idx))) return MEP_ERR_INVALID_ARG;
-  const size_t need = carve(nullptr, nullptr, nblk, R, E, B);
+  const size_t need = carve(nullptr, nullptr, nblk, R, E);
   if (workspace_bytes < need) return MEP_ERR_INVALID_ARG;
   PlanWs ws;
-  carve(&ws, static_cast<char*>(workspace), nblk, R, E, B);
+  carve(&ws, static_cast<char*>(workspace), nblk, R, E);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int tpt = tile_tokens(K);
 
-  const int hist_smem = (kTileAssign + E) * int(sizeof(int));
+  const int hist_smem = E * int(sizeof(int));
   const int offs_smem = (kTileAssign + kTileWarps * E) * int(sizeof(int));
-  const int npart = kPlanThreads > E ? kPlanThreads : E;
-  const int plan_smem = int(sizeof(int)) * (9 * (E + 1) + npart + 5 * (R + 1));
+  const int npart = 4 * kPlanThreads > E ? 4 * kPlanThreads : E;
+  const int plan_smem = int(sizeof(int)) * (9 * (E + 1) + (E + R) + npart + 5 * (R + 1));
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_hist), hist_smem) ||
       set_max_dynamic_smem(reinterpret_cast<const void*>(k_offsets), offs_smem) ||
       set_max_dynamic_smem(reinterpret_cast<const void*>(k_plan), plan_smem))
@@ -485,8 +553,11 @@ extern "C" int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int
 
   if (nblk > 0) k_hist<<<nblk, kTileThreads, hist_smem, st>>>(topk_idx, N, K, E, tpt, ws);
   PlanArgs pa{nblk, R, S, K, E, B, expert_counts, cu_seqlens, slot_expert, status, ws};
-  k_plan<<<1, kPlanThreads, plan_smem, st>>>(pa);
-  if (nblk > 0)
-    k_offsets<<<nblk, kTileThreads, offs_smem, st>>>(topk_idx, N, K, E, tpt, ws, status, dst_pos);
+  if (launch_pdl(k_plan, dim3(1), dim3(kPlanThreads), plan_smem, st, pa) != cudaSuccess)
+    return MEP_ERR_CUDA;
+  if (nblk > 0 &&
+      launch_pdl(k_offsets, dim3(nblk), dim3(kTileThreads), offs_smem, st, topk_idx, N, K, E,
+                 tpt, ws, static_cast<const int32_t*>(status), dst_pos) != cudaSuccess)
+    return MEP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }

@@ -37,6 +37,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
     k_reduce_grad(const int32_t* __restrict__ slot_expert, int E, int RB, long long HHp,
                   float* __restrict__ home, float* __restrict__ slot, int32_t* status) {
+  pdl_wait();
+  pdl_launch_dependents();
   if (read_status(status) != 0) return;
   extern __shared__ int smem[];
   int* s_cnt = smem;            // [E]   slots per expert
@@ -178,11 +180,10 @@ extern "C" int mep_reduce_grad(const int32_t* slot_expert, int E, int R, int B, 
   if (set_max_dynamic_smem(fn, smem)) return MEP_ERR_CUDA;
   const int grid = sm_count() * 4;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (vec)
-    k_reduce_grad<true><<<grid, kThreads, smem, st>>>(slot_expert, E, RB, HHp, home_grad,
-                                                      slot_grad, status);
-  else
-    k_reduce_grad<false><<<grid, kThreads, smem, st>>>(slot_expert, E, RB, HHp, home_grad,
-                                                       slot_grad, status);
-  return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
+  const cudaError_t err =
+      vec ? launch_pdl(k_reduce_grad<true>, dim3(grid), dim3(kThreads), smem, st, slot_expert, E,
+                       RB, (long long)HHp, home_grad, slot_grad, status)
+          : launch_pdl(k_reduce_grad<false>, dim3(grid), dim3(kThreads), smem, st, slot_expert,
+                       E, RB, (long long)HHp, home_grad, slot_grad, status);
+  return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
