@@ -12,13 +12,13 @@
 //   k_hist     grid over tiles of <= 2048 assignments: per-tile expert counts
 //              (shared-memory atomics) and routing checks, one token per
 //              thread.
-//   k_plan     one CTA: tile counts -> T_e and per-tile exclusive prefixes
-//              (16-byte column loads), home-first keep, overflow pour into
-//              deficits, slot table, cu_seqlens, per-expert row bases.
+//   k_plan     one CTA: tile counts -> T_e and per-group prefixes (16-byte
+//              column loads), home-first keep, overflow pour into deficits,
+//              slot table, cu_seqlens, per-expert row bases.
 //   k_offsets  grid over the same tiles: each assignment's index in its
-//              expert's token-ordered list (tile prefix + warp prefix + rank
-//              inside the warp from __match_any_sync), mapped to its
-//              destination row.
+//              expert's token-ordered list (group prefix + earlier tiles of
+//              the group + warp prefix + rank inside the warp from
+//              __match_any_sync), mapped to its destination row.
 // The planner's rule is home-first: a rank keeps, in expert order, at most
 // S*K of its home experts' tokens; the overflow segments, in expert order,
 // fill the under-loaded ranks' deficits in rank order, one slot per piece.
@@ -36,13 +36,15 @@ constexpr int kTileAssign = 2048;            // assignments per tile (upper boun
 constexpr int kWarpIters = kTileAssign / (32 * kTileWarps);  // 8 iterations per warp
 constexpr int kPlanThreads = 1024;           // k_plan block size
 constexpr int kMaxScanGroups = 64;           // tile groups in k_plan's prefix pass
+constexpr int kPartInts = 8192;              // k_plan shared ints for group sums
 
 // tokens per tile: as many as fit 2048 assignments, a multiple of 4 so that
 // every tile starts on a 16-byte boundary of topk_idx.
 inline int tile_tokens(int K) { return (kTileAssign / K) & ~3; }
 
 struct PlanWs {
-  int* blockhist;    // [nblk, E] tile counts, rewritten as tile exclusive prefixes
+  int* blockhist;    // [nblk, E] tile counts
+  int* groupbase;    // [kMaxScanGroups, E] count of e in all tiles before the group
   int* blockerr;     // [nblk]
   int* keep;         // [E] tokens kept on the home row
   int* home_base;    // [E] global row of the home row's first token
@@ -63,6 +65,7 @@ size_t carve(PlanWs* ws, char* base, int nblk, int R, int E) {
   PlanWs dummy;
   PlanWs* w = ws ? ws : &dummy;
   take(&w->blockhist, size_t(nblk) * E);
+  take(&w->groupbase, size_t(kMaxScanGroups) * E);
   take(&w->blockerr, size_t(nblk > 0 ? nblk : 1));
   take(&w->keep, E);
   take(&w->home_base, E);
@@ -172,17 +175,28 @@ template <> struct Vec<4> {
   }
 };
 
-// T_e and the per-tile exclusive prefixes of the tile counts, in place.
-// Columns are W experts wide; thread (g, c) owns tiles [g*tpg, (g+1)*tpg)
-// of column c.
+// Tiles are split into Gs groups of tpg consecutive tiles (tile_groups()).
+// tile_group_sums: T_e, and for every group g the count of e in all tiles
+// before g (groupbase). Each k_offsets CTA adds the few tiles of its own
+// group that precede it, so no single CTA reads every tile count twice.
+// Columns are W experts wide; thread (g, c) owns group g of column c.
+__host__ __device__ inline void tile_groups(int nblk, int E, int* Gs, int* tpg) {
+  int g = kPartInts / E;
+  if (g > kMaxScanGroups) g = kMaxScanGroups;
+  if (g > nblk) g = nblk;
+  if (g < 1) g = 1;
+  *Gs = g;
+  *tpg = nblk > 0 ? (nblk + g - 1) / g : 1;
+}
+
 template <int W>
-__device__ void tile_prefix(const PlanArgs& a, int* sPart, int* sT) {
+__device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT) {
   using V = typename Vec<W>::T;
   const int E = a.E, nblk = a.nblk, nthr = blockDim.x, tid = threadIdx.x;
   const int nc = E / W;
-  const int Gs = nc >= nthr ? 1 : min(kMaxScanGroups, nthr / nc);
-  const int tpg = (nblk + Gs - 1) / Gs;
-  V* h = reinterpret_cast<V*>(a.ws.blockhist);
+  int Gs, tpg;
+  tile_groups(nblk, E, &Gs, &tpg);
+  const V* h = reinterpret_cast<const V*>(a.ws.blockhist);
   for (int x = tid; x < Gs * nc; x += nthr) {
     const int g = x / nc, c = x - g * nc;
     const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
@@ -203,27 +217,13 @@ __device__ void tile_prefix(const PlanArgs& a, int* sPart, int* sT) {
     int run = 0;
     for (int g = 0; g < Gs; ++g) {
       const int v = sPart[g * E + e];
-      sPart[g * E + e] = run;
+      a.ws.groupbase[g * E + e] = run;
       run += v;
     }
     sT[e] = run;
     a.counts[e] = run;
   }
   __syncthreads();
-  for (int x = tid; x < Gs * nc; x += nthr) {
-    const int g = x / nc, c = x - g * nc;
-    const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
-    int run[W];
-#pragma unroll
-    for (int j = 0; j < W; ++j) run[j] = sPart[g * E + c * W + j];
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) {
-      const V v = h[size_t(b) * nc + c];
-      h[size_t(b) * nc + c] = Vec<W>::make(run);
-#pragma unroll
-      for (int j = 0; j < W; ++j) run[j] += Vec<W>::get(v, j);
-    }
-  }
 }
 
 // Exclusive scan of a short array by warp 0 (out may alias in; out[n] =
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
   const int EP = E + 1, RP = R + 1;
-  const int npart = max(4 * nthr, E);
+  const int npart = kPartInts;
   int* sT = smem;                // [E+1]
   int* sPre = sT + EP;           // [E+1]
   int* sKeep = sPre + EP;        // [E+1]
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   int* sPcBeg = sFlag + EP;      // [E+1]
   int* sPcCnt = sPcBeg + EP;     // [E+1]
   int* sPlen = sPcCnt + EP;      // [E+R] piece lengths, by global piece index
-  int* sPart = sPlen + E + R;    // [max(4*nthr, E)]
+  int* sPart = sPlen + E + R;    // [kPartInts] group sums
   int* sDef = sPart + npart;     // [R+1]
   int* sDst = sDef + RP;         // [R+1]
   int* sNp = sDst + RP;          // [R+1]
@@ -289,9 +289,9 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     return;
   }
 
-  // 1. T_e and per-tile exclusive prefixes
-  if ((E & 3) == 0) tile_prefix<4>(a, sPart, sT);
-  else tile_prefix<1>(a, sPart, sT);
+  // 1. T_e and the per-group prefixes of the tile counts
+  if ((E & 3) == 0) tile_group_sums<4>(a, sPart, sT);
+  else tile_group_sums<1>(a, sPart, sT);
 
   // 2. home-first keep: the count of e's earlier home experts is a
   //    difference of the running sum of T
@@ -408,7 +408,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
 // k_offsets: destination rows.
 __global__ void __launch_bounds__(kTileThreads)
     k_offsets(const int32_t* __restrict__ topk_idx, int N, int K, int E, int tok_per_tile,
-              PlanWs ws, const int32_t* __restrict__ status, int32_t* __restrict__ dst_pos) {
+              int nblk, PlanWs ws, const int32_t* __restrict__ status,
+              int32_t* __restrict__ dst_pos) {
   extern __shared__ int smem[];
   int* s_idx = smem;                    // [kTileAssign]
   int* s_wcnt = smem + kTileAssign;     // [kTileWarps, E]
@@ -460,9 +461,14 @@ __global__ void __launch_bounds__(kTileThreads)
   }
   __syncthreads();
   // per expert: exclusive prefix over warps, on top of the tile's prefix
-  const int* tile_pre = ws.blockhist + size_t(blk) * E;
+  // (the group's base plus the group's earlier tiles)
+  int Gs, tpg;
+  tile_groups(nblk, E, &Gs, &tpg);
+  const int g = blk / tpg;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = tile_pre[e];
+    int run = ws.groupbase[g * E + e];
+#pragma unroll 4
+    for (int b = g * tpg; b < blk; ++b) run += ws.blockhist[size_t(b) * E + e];
 #pragma unroll
     for (int w = 0; w < kTileWarps; ++w) {
       const int v = s_wcnt[w * E + e];
@@ -544,7 +550,7 @@ extern "C" int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int
 
   const int hist_smem = E * int(sizeof(int));
   const int offs_smem = (kTileAssign + kTileWarps * E) * int(sizeof(int));
-  const int npart = 4 * kPlanThreads > E ? 4 * kPlanThreads : E;
+  const int npart = kPartInts;
   const int plan_smem = int(sizeof(int)) * (9 * (E + 1) + (E + R) + npart + 5 * (R + 1));
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_hist), hist_smem) ||
       set_max_dynamic_smem(reinterpret_cast<const void*>(k_offsets), offs_smem) ||
@@ -557,7 +563,7 @@ extern "C" int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int
     return MEP_ERR_CUDA;
   if (nblk > 0 &&
       launch_pdl(k_offsets, dim3(nblk), dim3(kTileThreads), offs_smem, st, topk_idx, N, K, E,
-                 tpt, ws, static_cast<const int32_t*>(status), dst_pos) != cudaSuccess)
+                 tpt, nblk, ws, static_cast<const int32_t*>(status), dst_pos) != cudaSuccess)
     return MEP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
