@@ -272,6 +272,8 @@ def gpu_arm(args, rank: int, world: int, dist):
     total_ms = sum(times["step"])
     assert int(plan.status.item()) == 0
 
+    nxt = next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp) if rank == 0 else None
+
     # --- end to end through the public API with host buffers -------------
     idx_h = torch.from_numpy(idx).pin_memory()
     w_h = torch.from_numpy(w).pin_memory()
@@ -310,10 +312,75 @@ def gpu_arm(args, rank: int, world: int, dist):
     total_bytes = nb["plan"] + nb["dispatch"] + nb["combine"] + nb["reduce_grad"]
     t_max, e2e_max = max_over_ranks([total_ms, float(np.median(e2e_ms))], dist, dev)
     res = dict(
+        next_rows=nxt,
         total_ms=t_max, steps=args.steps, total_bytes=total_bytes, nb=nb, times=times,
         maxvio=maxvio, e2e_ms=e2e_max, h2d=h2d, d2h=d2h, clocks=clocks, sweep=sweep,
         t_wall=(t_wall0, t_wall1), shape=s, HHp=HHp,
     )
+    return res
+
+
+def next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp):
+    """Throughput of the steps beyond the forward/backward hot path on the
+    same workload: replica weight prefetch (bf16 E x H x H' weights, the
+    step's slot map) and the backward of dispatch and combine."""
+    import torch
+
+    import load_balancing_topk_gb300 as mep
+    from load_balancing_topk_gb300 import synth
+
+    peak, _ = measured_peak()
+    reps = 20
+
+    def timed(fn):
+        ts = []
+        for i in range(3 + reps):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    res = {}
+    se = plan.slot_expert
+    used = int((se >= 0).sum().item())
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    home_w = torch.randn((s.E, HHp), generator=g, device=dev).to(torch.bfloat16)
+    slot_w = torch.zeros((s.R, s.B, HHp), dtype=torch.bfloat16, device=dev)
+    ms = timed(lambda: mep.mep_prefetch(se, home_w, slot_w, plan.status, s.E))
+    nb = 2 * used * HHp * 2
+    res["prefetch"] = {"ms": round(ms, 4), "gbs": round(nb / ms / 1e6, 1),
+                       "frac_of_peak": round(nb / ms / 1e6 / peak, 4), "slots": used,
+                       "bytes": nb, "weights": f"bf16 [{s.E}, {synth.GRAD_H}x{synth.GRAD_HP}]"}
+    full = torch.from_numpy(synth.full_slot_map(s.E, s.R, s.B, seed=0)).to(dev)
+    ms = timed(lambda: mep.mep_prefetch(full, home_w, slot_w, None, s.E))
+    nb = 2 * s.R * s.B * HHp * 2
+    res["prefetch_all_slots"] = {"ms": round(ms, 4), "gbs": round(nb / ms / 1e6, 1),
+                                 "frac_of_peak": round(nb / ms / 1e6 / peak, 4),
+                                 "slots": s.R * s.B, "bytes": nb}
+    del home_w, slot_w
+    dh = torch.empty((s.N, s.H), dtype=torch.bfloat16, device=dev)
+    ms = timed(lambda: mep.mep_dispatch_backward(buf, plan.dst_pos, plan.status, s.R, s.S, s.K,
+                                                 dhidden=dh))
+    nb = s.A * s.H * 2 + s.N * s.H * 2 + 4 * s.A
+    res["dispatch_backward"] = {"ms": round(ms, 4), "gbs": round(nb / ms / 1e6, 1),
+                                "frac_of_peak": round(nb / ms / 1e6 / peak, 4), "bytes": nb}
+    dy = torch.empty((s.A, s.H), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((s.N, s.K), dtype=torch.float32, device=dev)
+    ms = timed(lambda: mep.mep_combine_backward(out, buf, w_d, plan.dst_pos, plan.status, s.R, s.S,
+                                                s.K, dy=dy, dw=dw))
+    nb = s.N * s.H * 2 + 2 * s.A * s.H * 2 + 16 * s.A
+    res["combine_backward"] = {"ms": round(ms, 4), "gbs": round(nb / ms / 1e6, 1),
+                               "frac_of_peak": round(nb / ms / 1e6 / peak, 4), "bytes": nb}
+    del dh, dy, dw
+    torch.cuda.synchronize()
+    assert int(plan.status.item()) == 0
+    res["note"] = "median of 20 reps after 3 warm-up, L2 flushed before each; same workload and plan"
     return res
 
 
@@ -567,6 +634,7 @@ def main():
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
         "sweep": res["sweep"],
+        "next_rows": res["next_rows"],
     }
     print(json.dumps(line), flush=True)
 

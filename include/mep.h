@@ -7,6 +7,8 @@
  *   mep_dispatch    fused permute into the static [R, S*K, H] buffer
  *   mep_combine     fused weighted unpermute back to [R*S, H]
  *   mep_reduce_grad redundant-slot gradients folded into home gradients
+ *   mep_prefetch    redundant experts' weights copied into their slots
+ *   mep_dispatch_backward / mep_combine_backward   the two permutes' gradients
  *
  * Sources (web pages about MoonEP, cited by title and section):
  *   "月之暗面开源MoonEP：面向MoE训练的专家并行通信库" -- sections
@@ -62,7 +64,7 @@ typedef uint16_t mep_bf16;
 #define MEP_ERR_CAPACITY 4      /* device: some rank needs more than B redundant slots */
 #define MEP_ERR_BAD_POSITION 5  /* device: a dst_pos entry outside [0, R*S*K) */
 #define MEP_ERR_BAD_SLOT_MAP 6  /* device: a slot_expert entry outside [-1, E) */
-#define MEP_ERR_TIMEOUT 7       /* device: a bounded wait inside a kernel gave up */
+#define MEP_ERR_TIMEOUT 7       /* device: a bounded wait gave up (reserved: no kernel waits today) */
 
 /* Size limits checked on the host. */
 #define MEP_MAX_E 4096     /* experts */
@@ -130,6 +132,26 @@ MEP_API int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int B,
              int32_t* dst_pos, int32_t* status, void* stream);
 
 /*
+ * mep_prefetch -- copy the planned redundant experts' weights into their
+ * slots ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库", 核心技术: the
+ * redundant experts' weights are prefetched before expert compute;
+ * 内存契约与权重布局: rows [E, E+B) of each rank's [E+B, H, H'] weight tensor
+ * are local prefetch slots):
+ *   slot_w[r][b][:] = home_w[slot_expert[r][b]][:]  for every slot != -1,
+ * a byte copy; unused slots are not touched. Any element type.
+ *   slot_expert  int32 [R, B]           from mep_plan (or any map into [-1, E))
+ *   expert_bytes int64                  bytes of one expert matrix (H*H'*elem), % 16 == 0
+ *   home_w       [E, expert_bytes]      home experts' weights (read only)
+ *   slot_w       [R, B, expert_bytes]   slot weights (written); must not overlap home_w
+ *   status       int32 [1]              read on entry (nonzero: no-op); set to
+ *                                       MEP_ERR_BAD_SLOT_MAP (nothing copied) if an
+ *                                       entry is outside [-1, E). May be NULL.
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG, MEP_ERR_CUDA.
+ */
+MEP_API int mep_prefetch(const int32_t* slot_expert, int E, int R, int B, int64_t expert_bytes,
+                         const void* home_w, void* slot_w, int32_t* status, void* stream);
+
+/*
  * mep_plan_static_scratch -- mep_plan without a caller-supplied workspace.
  * (The pages have no counterpart: this is an allocation-free variant of the
  * same planner for callers that cannot allocate device memory, such as a
@@ -190,6 +212,43 @@ MEP_API int mep_dispatch(const mep_bf16* hidden, const int32_t* dst_pos, int32_t
 MEP_API int mep_combine(const mep_bf16* y, const float* topk_w, const int32_t* dst_pos,
                 int32_t* status, int R, int S, int K, int H, mep_bf16* out,
                 void* stream);
+
+/*
+ * mep_dispatch_backward -- gradient of mep_dispatch: dispatch copies
+ * hidden[t] to the K rows dst_pos[t, k], so
+ *   dhidden[t, h] = bf16_rn( sum_{k=0..K-1} dbuf[dst_pos[t,k], h] )
+ * accumulated in fp32 from 0, one add per k in k order. (The pages name the
+ * fused permute/unpermute, "月之暗面开源MoonEP：面向MoE训练的专家并行通信库",
+ * 核心技术, but give no backward arithmetic; this is the same reading as
+ * combine's.)
+ *   dbuf     bf16 [R*S*K, H]   gradient of the dispatch buffer
+ *   dst_pos  int32 [R*S, K]    from mep_plan
+ *   status   int32 [1]         as for mep_dispatch; may be NULL
+ *   dhidden  bf16 [R*S, H]     output; must not overlap dbuf
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG, MEP_ERR_CUDA.
+ */
+MEP_API int mep_dispatch_backward(const mep_bf16* dbuf, const int32_t* dst_pos, int32_t* status,
+                                  int R, int S, int K, int H, mep_bf16* dhidden, void* stream);
+
+/*
+ * mep_combine_backward -- gradients of mep_combine (same section):
+ *   dy[dst_pos[t,k], h] = bf16_rn( fp32(topk_w[t,k] * dout[t,h]) )
+ *   dw[t, k]            = sum_h dout[t,h] * y[dst_pos[t,k], h]   (fp32)
+ * Every bf16 x bf16 product is exact in fp32; the dw sum is accumulated in
+ * fp32 (per lane, then across a warp), so it matches the exact dot product to
+ * within (H/32 + 6) * 2^-24 * sum_h |dout[t,h] * y[dst_pos[t,k],h]|.
+ *   dout     bf16 [R*S, H]     gradient of combine's output
+ *   y        bf16 [R*S*K, H]   combine's input (expert outputs)
+ *   topk_w   fp32 [R*S, K]     routing weights
+ *   dst_pos  int32 [R*S, K]    from mep_plan
+ *   status   int32 [1]         as for mep_dispatch; may be NULL
+ *   dy       bf16 [R*S*K, H]   output, every row written; must not overlap y or dout
+ *   dw       fp32 [R*S, K]     output
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG, MEP_ERR_CUDA.
+ */
+MEP_API int mep_combine_backward(const mep_bf16* dout, const mep_bf16* y, const float* topk_w,
+                                 const int32_t* dst_pos, int32_t* status, int R, int S, int K,
+                                 int H, mep_bf16* dy, float* dw, void* stream);
 
 /*
  * mep_reduce_grad -- fold redundant-slot gradients into home gradients

@@ -15,7 +15,10 @@ Entry points (same names as the C ABI):
 * :func:`mep_dispatch` -- fused permute into the static [R, S*K, H] buffer;
 * :func:`mep_combine` -- fused weighted unpermute back to [R*S, H];
 * :func:`mep_reduce_grad` -- slot gradients into home gradients, consumed
-  slots zeroed.
+  slots zeroed;
+* :func:`mep_prefetch` -- redundant experts' weights copied into their slots;
+* :func:`mep_dispatch_backward` / :func:`mep_combine_backward` -- gradients of
+  the two permutes.
 """
 
 from __future__ import annotations
@@ -28,7 +31,7 @@ from typing import NamedTuple, Optional
 __all__ = [
     "MepError", "Plan", "library_path", "load_library", "status_string", "version",
     "plan_workspace_bytes", "mep_plan", "mep_dispatch", "mep_combine", "mep_reduce_grad",
-    "STATUS",
+    "mep_prefetch", "mep_dispatch_backward", "mep_combine_backward", "STATUS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -61,6 +64,9 @@ SIGNATURES = [
     ("mep_dispatch", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
     ("mep_combine", _I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
     ("mep_reduce_grad", _I, [_VP, _I, _I, _I, ctypes.c_int64, _VP, _VP, _VP, _VP]),
+    ("mep_prefetch", _I, [_VP, _I, _I, _I, ctypes.c_int64, _VP, _VP, _VP, _VP]),
+    ("mep_dispatch_backward", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
+    ("mep_combine_backward", _I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP]),
 ]
 
 
@@ -268,3 +274,88 @@ def mep_reduce_grad(slot_expert, home_grad, slot_grad, status, E: int):
                                             _ptr(slot_grad), _ptr(status), _stream(dev))
     _check("mep_reduce_grad", rc)
     return home_grad, slot_grad
+
+
+def mep_prefetch(slot_expert, home_w, slot_w, status, E: int):
+    """slot_w[r, b] = home_w[slot_expert[r, b]] for every used slot (in place).
+
+    home_w: [E, ...]; slot_w: [R, B, ...] with the same dtype and trailing
+    size; slot_expert: int32 [R, B]. Any dtype (the copy is bytewise).
+    """
+    torch = _torch()
+    _need(slot_expert, "slot_expert", torch.int32)
+    R, B = slot_expert.shape
+    dev = slot_expert.device
+    _need(home_w, "home_w", home_w.dtype, None, dev)
+    _need(slot_w, "slot_w", home_w.dtype, None, dev)
+    nbytes = home_w.numel() * home_w.element_size()
+    if nbytes % E:
+        raise ValueError("home_w must be [E, ...]")
+    per = nbytes // E
+    if slot_w.numel() * slot_w.element_size() != R * B * per:
+        raise ValueError("slot_w must be [R, B, ...] with home_w's trailing size")
+    if status is not None:
+        _need(status, "status", torch.int32, (1,), dev)
+    with torch.cuda.device(dev):
+        rc = load_library().mep_prefetch(_ptr(slot_expert), E, R, B, per, _ptr(home_w),
+                                         _ptr(slot_w), _ptr(status), _stream(dev))
+    _check("mep_prefetch", rc)
+    return slot_w
+
+
+def mep_dispatch_backward(dbuf, dst_pos, status, R: int, S: int, K: int, dhidden=None):
+    """dhidden[t] = bf16(sum_k dbuf[dst_pos[t, k]]) (fp32 adds in k order)."""
+    torch = _torch()
+    _need(dbuf, "dbuf", torch.bfloat16)
+    H = dbuf.shape[-1]
+    N = R * S
+    if dbuf.numel() != N * K * H:
+        raise ValueError("dbuf must hold R*S*K rows of H")
+    dev = dbuf.device
+    _need(dst_pos, "dst_pos", torch.int32, (N, K), dev)
+    if status is not None:
+        _need(status, "status", torch.int32, (1,), dev)
+    if dhidden is None:
+        dhidden = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    else:
+        _need(dhidden, "dhidden", torch.bfloat16, (N, H), dev)
+    with torch.cuda.device(dev):
+        rc = load_library().mep_dispatch_backward(_ptr(dbuf), _ptr(dst_pos), _ptr(status), R, S, K,
+                                                  H, _ptr(dhidden), _stream(dev))
+    _check("mep_dispatch_backward", rc)
+    return dhidden
+
+
+def mep_combine_backward(dout, y, topk_w, dst_pos, status, R: int, S: int, K: int, dy=None,
+                         dw=None):
+    """(dy, dw) with dy[dst_pos[t,k]] = bf16(w[t,k] * dout[t]) and
+    dw[t,k] = <dout[t], y[dst_pos[t,k]]> (fp32)."""
+    torch = _torch()
+    _need(dout, "dout", torch.bfloat16)
+    N, H = dout.shape
+    if N != R * S:
+        raise ValueError("dout must be [R*S, H]")
+    dev = dout.device
+    _need(y, "y", torch.bfloat16, None, dev)
+    if y.numel() != N * K * H:
+        raise ValueError("y must hold R*S*K rows of H")
+    _need(topk_w, "topk_w", torch.float32, (N, K), dev)
+    _need(dst_pos, "dst_pos", torch.int32, (N, K), dev)
+    if status is not None:
+        _need(status, "status", torch.int32, (1,), dev)
+    if dy is None:
+        dy = torch.empty((N * K, H), dtype=torch.bfloat16, device=dev)
+    else:
+        _need(dy, "dy", torch.bfloat16, None, dev)
+        if dy.numel() != N * K * H:
+            raise ValueError("dy must hold R*S*K rows of H")
+    if dw is None:
+        dw = torch.empty((N, K), dtype=torch.float32, device=dev)
+    else:
+        _need(dw, "dw", torch.float32, (N, K), dev)
+    with torch.cuda.device(dev):
+        rc = load_library().mep_combine_backward(_ptr(dout), _ptr(y), _ptr(topk_w), _ptr(dst_pos),
+                                                 _ptr(status), R, S, K, H, _ptr(dy), _ptr(dw),
+                                                 _stream(dev))
+    _check("mep_combine_backward", rc)
+    return dy, dw

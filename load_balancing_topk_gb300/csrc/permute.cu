@@ -1,4 +1,5 @@
-// permute.cu -- fused permute (mep_dispatch) and weighted unpermute (mep_combine).
+// permute.cu -- fused permute (mep_dispatch), weighted unpermute (mep_combine)
+// and their backward passes (mep_dispatch_backward, mep_combine_backward).
 //
 // Source: "月之暗面开源MoonEP：面向MoE训练的专家并行通信库", section 核心技术
 // (零拷贝与静态形状: tokens are written straight into preset, expert-grouped
@@ -136,8 +137,10 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
 }
 
 // KT > 0: K known at compile time (all K gathers of a vector in flight at
-// once). KT == 0: any K, gathered in batches of 8.
-template <int KT>
+// once). KT == 0: any K, gathered in batches of 8. UNIT: every weight is 1
+// and topk_w is not read (the backward of dispatch: sum of the K rows; an fma
+// with 1 rounds exactly like an add).
+template <int KT, bool UNIT = false>
 __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
     k_combine(const uint4* __restrict__ y, const float* __restrict__ topk_w,
               const int32_t* __restrict__ dst_pos, int32_t* status, long long N, int Kr,
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
   for (long long t = warp0; t < N; t += nwarp) {
     const int r0 = lane < K ? __ldg(dst_pos + t * K + lane) : 0;
     const int r1 = lane + 32 < K ? __ldg(dst_pos + t * K + lane + 32) : 0;
-    const float w0 = lane < K ? __ldg(topk_w + t * K + lane) : 0.f;
+    const float w0 = UNIT ? 1.f : (lane < K ? __ldg(topk_w + t * K + lane) : 0.f);
     const bool bad = (lane < K && (r0 < 0 || r0 >= nrows)) ||
                      (lane + 32 < K && (r1 < 0 || r1 >= nrows));
     if (__any_sync(MEP_FULL_MASK, bad)) {
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
             const int k = k0 + j;
             if (k < K) {
               const long long row = __ldg(dst_pos + t * K + k);
-              ws[j] = __ldg(topk_w + t * K + k);
+              ws[j] = UNIT ? 1.f : __ldg(topk_w + t * K + k);
               q[j] = __ldg(y + row * vpr + v);
             }
           }
@@ -202,15 +205,130 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
   }
 }
 
-template <int KT>
+template <int KT, bool UNIT = false>
 cudaError_t launch_combine(const uint4* y, const float* w, const int32_t* dst, int32_t* status,
                            long long N, int K, long long vpr, long long nrows, uint4* out,
                            cudaStream_t st) {
   const long long want = (N + MEP_COMBINE_WARPS - 1) / MEP_COMBINE_WARPS;
   const long long cap = (long long)sm_count() * 64;
   const int grid = int(want < cap ? want : cap);
-  return launch_pdl(k_combine<KT>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0, st, y, w, dst,
-                    status, N, K, vpr, nrows, out);
+  return launch_pdl(k_combine<KT, UNIT>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0, st, y, w,
+                    dst, status, N, K, vpr, nrows, out);
+}
+
+// ---------------------------------------------------------------------------
+// Backward of combine, one warp per token. Per 16-byte column vector v: load
+// dout[t, v] and the K rows y[dst_pos[t,k], v]; write
+//   dy[dst_pos[t,k], v] = bf16_rn(fp32(w[t,k] * dout[t, v]))   (streaming)
+// and accumulate the K dot products <dout[t], y[dst_pos[t,k]]> per lane with
+// fp32 fma (every bf16 x bf16 product is exact in fp32), then reduce them
+// across the warp (butterfly) and write dw[t, k] from lane 0.
+__device__ __forceinline__ uint4 scale8(float w, uint4 q) {
+  const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = __fmul_rn(w, __uint_as_float(v[j] << 16));
+    const float hi = __fmul_rn(w, __uint_as_float(v[j] & 0xffff0000u));
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    o[j] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float dot8(float acc, uint4 a, uint4 b) {
+  const uint32_t va[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t vb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    acc = __fmaf_rn(__uint_as_float(va[j] << 16), __uint_as_float(vb[j] << 16), acc);
+    acc = __fmaf_rn(__uint_as_float(va[j] & 0xffff0000u), __uint_as_float(vb[j] & 0xffff0000u), acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(MEP_FULL_MASK, v, d);
+  return v;
+}
+
+template <int KT>
+__global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
+    k_combine_backward(const uint4* __restrict__ dout, const uint4* __restrict__ y,
+                       const float* __restrict__ topk_w, const int32_t* __restrict__ dst_pos,
+                       int32_t* status, long long N, int Kr, long long vpr, long long nrows,
+                       uint4* __restrict__ dy, float* __restrict__ dw) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (read_status(status) != 0) return;
+  const int K = KT > 0 ? KT : Kr;
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = (long long)blockIdx.x * MEP_COMBINE_WARPS + (threadIdx.x >> 5);
+  const long long nwarp = (long long)gridDim.x * MEP_COMBINE_WARPS;
+  for (long long t = warp0; t < N; t += nwarp) {
+    const int r0 = lane < K ? __ldg(dst_pos + t * K + lane) : 0;
+    const int r1 = lane + 32 < K ? __ldg(dst_pos + t * K + lane + 32) : 0;
+    const float w0 = lane < K ? __ldg(topk_w + t * K + lane) : 0.f;
+    const bool bad = (lane < K && (r0 < 0 || r0 >= nrows)) ||
+                     (lane + 32 < K && (r1 < 0 || r1 >= nrows));
+    if (__any_sync(MEP_FULL_MASK, bad)) {
+      if (lane == 0) set_status(status, MEP_ERR_BAD_POSITION);
+      continue;
+    }
+    const uint4* d = dout + t * vpr;
+    if constexpr (KT > 0) {
+      long long rows[KT];
+      float ws[KT], acc[KT];
+#pragma unroll
+      for (int k = 0; k < KT; ++k) {
+        rows[k] = (long long)__shfl_sync(MEP_FULL_MASK, r0, k) * vpr;
+        ws[k] = __shfl_sync(MEP_FULL_MASK, w0, k);
+        acc[k] = 0.f;
+      }
+      for (long long v = lane; v < vpr; v += 32) {
+        const uint4 g = __ldg(d + v);
+        uint4 q[KT];
+#pragma unroll
+        for (int k = 0; k < KT; ++k) q[k] = __ldg(y + rows[k] + v);
+#pragma unroll
+        for (int k = 0; k < KT; ++k) {
+          __stcs(dy + rows[k] + v, scale8(ws[k], g));
+          acc[k] = dot8(acc[k], g, q[k]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < KT; ++k) {
+        const float s = warp_sum(acc[k]);
+        if (lane == 0) dw[t * K + k] = s;
+      }
+    } else {
+      for (int k = 0; k < K; ++k) {
+        const long long row = (long long)__ldg(dst_pos + t * K + k) * vpr;
+        const float wk = __ldg(topk_w + t * K + k);
+        float acc = 0.f;
+        for (long long v = lane; v < vpr; v += 32) {
+          const uint4 g = __ldg(d + v);
+          __stcs(dy + row + v, scale8(wk, g));
+          acc = dot8(acc, g, __ldg(y + row + v));
+        }
+        const float s = warp_sum(acc);
+        if (lane == 0) dw[t * K + k] = s;
+      }
+    }
+  }
+}
+
+template <int KT>
+cudaError_t launch_combine_backward(const uint4* dout, const uint4* y, const float* w,
+                                    const int32_t* dst, int32_t* status, long long N, int K,
+                                    long long vpr, long long nrows, uint4* dy, float* dw,
+                                    cudaStream_t st) {
+  const long long want = (N + MEP_COMBINE_WARPS - 1) / MEP_COMBINE_WARPS;
+  const long long cap = (long long)sm_count() * 64;
+  const int grid = int(want < cap ? want : cap);
+  return launch_pdl(k_combine_backward<KT>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0, st,
+                    dout, y, w, dst, status, N, K, vpr, nrows, dy, dw);
 }
 
 }  // namespace
@@ -272,6 +390,57 @@ extern "C" int mep_combine(const mep_bf16* y, const float* topk_w, const int32_t
     case 6: err = launch_combine<6>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
     case 8: err = launch_combine<8>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
     default: err = launch_combine<0>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+  }
+  return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
+}
+
+extern "C" int mep_dispatch_backward(const mep_bf16* dbuf, const int32_t* dst_pos,
+                                     int32_t* status, int R, int S, int K, int H,
+                                     mep_bf16* dhidden, void* stream) {
+  int rc = permute_check(dbuf, dhidden, dst_pos, R, S, K, H);
+  if (rc != MEP_OK) return rc;
+  const long long N = (long long)R * S;
+  if (N == 0) return MEP_OK;
+  const long long vpr = H / 8;
+  const uint4* g4 = reinterpret_cast<const uint4*>(dbuf);
+  uint4* o4 = reinterpret_cast<uint4*>(dhidden);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long nrows = N * K;
+  cudaError_t err;
+  switch (K) {
+    case 1: err = launch_combine<1, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+    case 2: err = launch_combine<2, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+    case 4: err = launch_combine<4, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+    case 6: err = launch_combine<6, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+    case 8: err = launch_combine<8, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+    default: err = launch_combine<0, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+  }
+  return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
+}
+
+extern "C" int mep_combine_backward(const mep_bf16* dout, const mep_bf16* y, const float* topk_w,
+                                    const int32_t* dst_pos, int32_t* status, int R, int S, int K,
+                                    int H, mep_bf16* dy, float* dw, void* stream) {
+  int rc = permute_check(dout, y, dst_pos, R, S, K, H);
+  if (rc != MEP_OK) return rc;
+  const long long N = (long long)R * S;
+  if (N == 0) return MEP_OK;
+  if (topk_w == nullptr || dy == nullptr || dw == nullptr || !aligned16(dy))
+    return MEP_ERR_INVALID_ARG;
+  const long long vpr = H / 8;
+  const uint4* d4 = reinterpret_cast<const uint4*>(dout);
+  const uint4* y4 = reinterpret_cast<const uint4*>(y);
+  uint4* dy4 = reinterpret_cast<uint4*>(dy);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long nrows = N * K;
+  cudaError_t err;
+  switch (K) {
+    case 1: err = launch_combine_backward<1>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
+    case 2: err = launch_combine_backward<2>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
+    case 4: err = launch_combine_backward<4>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
+    case 6: err = launch_combine_backward<6>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
+    case 8: err = launch_combine_backward<8>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
+    default: err = launch_combine_backward<0>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
   }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }

@@ -14,7 +14,12 @@ the step list and citations):
 * :func:`dispatch` / :func:`combine` -- the fused permute / weighted unpermute
   (section 核心技术, 零拷贝与静态形状);
 * :func:`reduce_grad` -- slot gradients into home gradients, consumed slots
-  zeroed (section 内存契约与权重布局, gradient paragraph).
+  zeroed (section 内存契约与权重布局, gradient paragraph);
+* :func:`prefetch` -- redundant slots receive a copy of their expert's home
+  weights (sections 核心技术 and 内存契约与权重布局);
+* :func:`dispatch_backward` / :func:`combine_backward` -- the gradients of the
+  fused permute and of the weighted unpermute (section 核心技术 names the
+  pair; their arithmetic is this library's reading, stated in oracle.c).
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (closed forms, brute force, an independent lexsort derivation, hand-worked
@@ -75,6 +80,16 @@ def _load():
             lib.orc_reduce_grad.restype = ctypes.c_int
             lib.orc_reduce_grad.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, c_i64,
                                             ctypes.c_void_p, ctypes.c_void_p]
+            lib.orc_prefetch.restype = ctypes.c_int
+            lib.orc_prefetch.argtypes = [i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, c_i64,
+                                         ctypes.c_void_p, ctypes.c_void_p]
+            lib.orc_dispatch_backward.restype = None
+            lib.orc_dispatch_backward.argtypes = [ctypes.c_void_p, i32p, c_i64, ctypes.c_int, c_i64,
+                                                  ctypes.c_void_p]
+            lib.orc_combine_backward.restype = None
+            lib.orc_combine_backward.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, i32p,
+                                                 c_i64, ctypes.c_int, c_i64, ctypes.c_void_p,
+                                                 ctypes.c_void_p]
             lib.orc_f32_to_bf16_array.restype = None
             lib.orc_f32_to_bf16_array.argtypes = [ctypes.c_void_p, c_i64, ctypes.c_void_p]
             _lib = lib
@@ -178,6 +193,48 @@ def reduce_grad(slot_expert: np.ndarray, home: np.ndarray, slot: np.ndarray, E: 
     assert h.size == E * HHp and s.size == R * B * HHp
     st = _load().orc_reduce_grad(_i32(se), E, R, B, HHp, h.ctypes.data, s.ctypes.data)
     return STATUS[st], h, s
+
+
+def prefetch(slot_expert: np.ndarray, home: np.ndarray, slot: np.ndarray, E: int):
+    """Returns (status, slot') without touching the inputs: slot'[s] = home[slot_expert[s]]
+    (a byte copy) for every used slot, unused slots unchanged. home is [E, ...], slot is
+    [R*B, ...] of the same dtype and trailing size."""
+    se = np.ascontiguousarray(slot_expert, dtype=np.int32)
+    R, B = se.shape
+    h = np.ascontiguousarray(home)
+    s = np.array(slot, copy=True, order="C")
+    nbytes = h.nbytes // E
+    assert h.nbytes == E * nbytes and s.nbytes == R * B * nbytes and h.dtype == s.dtype
+    st = _load().orc_prefetch(_i32(se), E, R, B, nbytes, h.ctypes.data, s.ctypes.data)
+    return STATUS[st], s
+
+
+def dispatch_backward(dbuf: np.ndarray, dst_pos: np.ndarray) -> np.ndarray:
+    """dhidden[t] = bf16(sum_k fp32 dbuf[dst_pos[t, k]]), adds in k order."""
+    dbuf = np.ascontiguousarray(dbuf, dtype=np.uint16)
+    dst_pos = np.ascontiguousarray(dst_pos, dtype=np.int32)
+    N, K = dst_pos.shape
+    H = dbuf.shape[1]
+    out = np.empty((N, H), dtype=np.uint16)
+    _load().orc_dispatch_backward(dbuf.ctypes.data, _i32(dst_pos), N, K, H, out.ctypes.data)
+    return out
+
+
+def combine_backward(dout: np.ndarray, y: np.ndarray, w: np.ndarray, dst_pos: np.ndarray):
+    """(dy bf16 [A, H], dw float64 [N, K]) of out[t] = sum_k w[t,k] y[dst_pos[t,k]].
+
+    Rows of dy that no assignment maps to are left 0."""
+    dout = np.ascontiguousarray(dout, dtype=np.uint16)
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    dst_pos = np.ascontiguousarray(dst_pos, dtype=np.int32)
+    N, K = dst_pos.shape
+    H = dout.shape[1]
+    dy = np.zeros_like(y)
+    dw = np.empty((N, K), dtype=np.float64)
+    _load().orc_combine_backward(dout.ctypes.data, y.ctypes.data, w.ctypes.data, _i32(dst_pos), N, K,
+                                 H, dy.ctypes.data, dw.ctypes.data)
+    return dy, dw
 
 
 def f32_to_bf16(x: np.ndarray) -> np.ndarray:

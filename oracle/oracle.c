@@ -361,3 +361,66 @@ void orc_f32_to_bf16_array(const float* x, int64_t n, uint16_t* out) {
   int64_t i;
   for (i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(x[i]);
 }
+
+/* Replica weight prefetch ([umios] 核心技术: the weights of the planned
+ * redundant experts are fetched before expert compute; 内存契约与权重布局:
+ * rows [E, E+B) of each rank's [E+B, H, H'] weight tensor are local prefetch
+ * slots). For every slot with slot_expert[r][b] = e != -1, slot[r][b] is a
+ * byte copy of home[e]; unused slots are not touched. home is [E, nbytes],
+ * slot is [R*B, nbytes]. Returns ORC_BAD_ROUTING (and copies nothing) if an
+ * entry is neither -1 nor in [0, E). */
+int orc_prefetch(const int32_t* slot_expert, int E, int R, int B, int64_t nbytes,
+                 const uint8_t* home, uint8_t* slot) {
+  int s;
+  for (s = 0; s < R * B; ++s)
+    if (slot_expert[s] < -1 || slot_expert[s] >= E) return ORC_BAD_ROUTING;
+  for (s = 0; s < R * B; ++s)
+    if (slot_expert[s] >= 0)
+      memcpy(slot + (int64_t)s * nbytes, home + (int64_t)slot_expert[s] * nbytes, (size_t)nbytes);
+  return ORC_OK;
+}
+
+/* Backward of the fused permute (dispatch): dispatch copies hidden[t] to the
+ * K rows dst_pos[t, k], so dhidden[t, h] = sum_k dbuf[dst_pos[t, k], h]. The
+ * pages give no backward arithmetic ([umios] 核心技术 names the fused
+ * permute/unpermute only); this library's reading mirrors combine: fp32 from
+ * 0, one add per k in k order, round to nearest-even bf16. */
+void orc_dispatch_backward(const uint16_t* dbuf, const int32_t* dst_pos, int64_t N, int K,
+                           int64_t H, uint16_t* dhidden) {
+  int64_t t, h;
+  int k;
+  for (t = 0; t < N; ++t)
+    for (h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      for (k = 0; k < K; ++k) acc = acc + orc_bf16_to_f32(dbuf[(int64_t)dst_pos[t * K + k] * H + h]);
+      dhidden[t * H + h] = orc_f32_to_bf16(acc);
+    }
+}
+
+/* Backward of the weighted unpermute (combine): out[t] = sum_k w[t,k] *
+ * y[dst_pos[t,k]], so
+ *   dy[dst_pos[t,k], h] = w[t,k] * dout[t,h]   (an fp32 product, then nearest-
+ *                                               even bf16, this library's reading)
+ *   dw[t,k] = sum_h dout[t,h] * y[dst_pos[t,k], h]
+ * dw is the plain definition, accumulated in double: every product of two
+ * bf16 values is exact in double, so the result is the dot product to
+ * within double rounding. */
+void orc_combine_backward(const uint16_t* dout, const uint16_t* y, const float* w,
+                          const int32_t* dst_pos, int64_t N, int K, int64_t H, uint16_t* dy,
+                          double* dw) {
+  int64_t t, h;
+  int k;
+  for (t = 0; t < N; ++t)
+    for (k = 0; k < K; ++k) {
+      const int64_t row = dst_pos[t * K + k];
+      const float wk = w[t * K + k];
+      double acc = 0.0;
+      for (h = 0; h < H; ++h) {
+        const float d = orc_bf16_to_f32(dout[t * H + h]);
+        const float p = wk * d;
+        dy[row * H + h] = orc_f32_to_bf16(p);
+        acc += (double)d * (double)orc_bf16_to_f32(y[row * H + h]);
+      }
+      dw[t * K + k] = acc;
+    }
+}

@@ -111,3 +111,13 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mep, "_PKG", str(tmp_path))
     with pytest.raises(RuntimeError, match="missing"):
         mep.load_library()
+
+
+def test_prefetch_rejects_bad_args(lib):
+    bad = mep.STATUS_CODE["MEP_ERR_INVALID_ARG"]
+    assert lib.mep_prefetch(16, 0, 2, 2, 64, 16, 16, None, None) == bad     # E < 1
+    assert lib.mep_prefetch(16, 4, 2, 2, 24, 16, 16, None, None) == bad     # bytes % 16
+    assert lib.mep_prefetch(16, 4, 2, 2, -16, 16, 16, None, None) == bad    # bytes < 0
+    assert lib.mep_prefetch(None, 4, 2, 2, 64, 16, 16, None, None) == bad   # null map
+    assert lib.mep_prefetch(16, 4, 2, 2, 64, 24, 16, None, None) == bad     # misaligned
+    assert lib.mep_prefetch(None, 4, 2, 0, 64, None, None, None, None) == 0  # no slots

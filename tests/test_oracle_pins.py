@@ -377,3 +377,112 @@ def test_home_first_against_optimum_on_tiny_instances():
         assert opt is not None and p["n_pieces"] >= opt
         ratios.append((p["n_pieces"], opt))
     print("home-first pieces vs optimum:", ratios)
+
+
+# --------------------------------------------------------------------------
+# replica weight prefetch
+def test_prefetch_is_fancy_indexing_copy():
+    E, R, B, n = 8, 4, 3, 37
+    se = np.array([[4, 6, -1], [0, 6, 7], [-1, -1, -1], [2, 6, 1]], dtype=np.int32)
+    rng = np.random.default_rng(3)
+    home = rng.integers(0, 2**16, size=(E, n), dtype=np.uint64).astype(np.uint16)
+    slot = rng.integers(0, 2**16, size=(R * B, n), dtype=np.uint64).astype(np.uint16)
+    st, got = oracle.prefetch(se, home, slot, E)
+    assert st == "ok"
+    used = se.reshape(-1) >= 0
+    np.testing.assert_array_equal(got[used], home[se.reshape(-1)[used]])
+    np.testing.assert_array_equal(got[~used], slot[~used])
+
+
+def test_prefetch_rejects_bad_map():
+    se = np.array([[1, 9]], dtype=np.int32)
+    home = np.ones((4, 8), np.float32)
+    slot = np.zeros((2, 8), np.float32)
+    st, got = oracle.prefetch(se, home, slot, 4)
+    assert st == "bad_routing" and (got == 0).all()
+
+
+# --------------------------------------------------------------------------
+# backward of dispatch and combine
+def _hex_fixture(name):
+    f = {}
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            if line.strip() and not line.startswith("#"):
+                k, *v = line.split()
+                f[k] = v
+    return f
+
+
+def test_dispatch_backward_order_fixture():
+    f = _hex_fixture("dispatch_backward_order.txt")
+    dbuf = np.array([int(x, 16) for x in f["dbuf_bits"]], dtype=np.uint16).reshape(3, 1)
+    dst = np.array([int(x) for x in f["dst_pos"]], dtype=np.int32).reshape(1, 3)
+    got = oracle.dispatch_backward(dbuf, dst)
+    assert got.reshape(-1).tolist() == [int(x, 16) for x in f["dhidden_bits"]]
+
+
+def test_combine_backward_rounding_fixture():
+    f = _hex_fixture("combine_backward_rounding.txt")
+    w = np.array([int(f["w_bits"][0], 16)], dtype=np.uint32).view(np.float32).reshape(1, 1)
+    dout = np.array([int(f["dout_bits"][0], 16)], dtype=np.uint16).reshape(1, 1)
+    y = np.zeros((1, 1), np.uint16)
+    dy, dw = oracle.combine_backward(dout, y, w, np.zeros((1, 1), np.int32))
+    assert dy.reshape(-1).tolist() == [int(f["dy_bits"][0], 16)]
+
+
+def test_dispatch_backward_k1_is_gather_and_integers_exact():
+    shape = synth.Shape(R=2, E=4, K=1, S=30, H=16, B=2)
+    idx, _ = synth.routing(shape, seed=1, alpha=1.0)
+    p = oracle.plan(idx, 2, 30, 1, 4, 2)
+    dbuf = synth.bf16_normal(shape.A, shape.H, seed=9, tag=41)
+    got = oracle.dispatch_backward(dbuf, p["dst_pos"])
+    np.testing.assert_array_equal(got, dbuf[p["dst_pos"][:, 0]])
+    # small integers: every partial sum exact, so any order gives the integer sum
+    N, K, H = 20, 4, 8
+    vals = synth.integer_valued((N * K, H), seed=4).astype(np.float32)
+    dbuf = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    dst = np.random.default_rng(0).permutation(N * K).astype(np.int32).reshape(N, K)
+    got = oracle.bf16_to_f32(oracle.dispatch_backward(dbuf, dst))
+    np.testing.assert_array_equal(got, vals[dst].sum(axis=1))
+
+
+def test_dispatch_backward_is_adjoint_of_dispatch():
+    # <dispatch(x), g> == <x, dispatch_backward(g)> for integer-valued x, g (exact)
+    shape = synth.Shape(R=2, E=6, K=3, S=40, H=8, B=3)
+    idx, _ = synth.routing(shape, seed=2, alpha=1.0)
+    p = oracle.plan(idx, 2, 40, 3, 6, 3)
+    xv = synth.integer_valued((shape.N, shape.H), seed=5, lo=-3, hi=3)
+    gv = synth.integer_valued((shape.A, shape.H), seed=6, lo=-3, hi=3)
+    to16 = lambda a: torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    buf = oracle.bf16_to_f32(oracle.dispatch(to16(xv), p["dst_pos"], shape.A)).astype(np.float64)
+    dx = oracle.bf16_to_f32(oracle.dispatch_backward(to16(gv), p["dst_pos"])).astype(np.float64)
+    assert (buf * gv).sum() == (xv.astype(np.float64) * dx).sum()
+
+
+def test_combine_backward_dy_and_dw():
+    import math
+
+    shape = synth.Shape(R=2, E=8, K=4, S=25, H=64, B=4)
+    idx, w = synth.routing(shape, seed=3, alpha=0.5)
+    p = oracle.plan(idx, 2, 25, 4, 8, 4)
+    dout = synth.bf16_normal(shape.N, shape.H, seed=3, tag=51)
+    y = synth.bf16_normal(shape.A, shape.H, seed=3, tag=52)
+    dy, dw = oracle.combine_backward(dout, y, w, p["dst_pos"])
+    d32 = oracle.bf16_to_f32(dout)
+    y32 = oracle.bf16_to_f32(y)
+    # dw against an exactly rounded sum of the (exact) products
+    for t in range(shape.N):
+        for k in range(shape.K):
+            prods = [float(a) * float(b) for a, b in zip(d32[t], y32[p["dst_pos"][t, k]])]
+            assert abs(dw[t, k] - math.fsum(prods)) <= 1e-12 * (sum(abs(q) for q in prods) + 1e-30)
+    # dy: unit weights and K = 1 give the rows of dout back exactly
+    dy1, _ = oracle.combine_backward(dout, y[: shape.N], np.ones((shape.N, 1), np.float32),
+                                     np.arange(shape.N, dtype=np.int32)[::-1].reshape(-1, 1).copy())
+    np.testing.assert_array_equal(dy1[::-1], dout)
+    # dyadic weights: products exact in fp32, so dy = bf16(w * dout) rounds once
+    wd = np.full((shape.N, shape.K), 0.25, np.float32)
+    dyd, _ = oracle.combine_backward(dout, y, wd, p["dst_pos"])
+    want = torch.from_numpy(d32 * np.float32(0.25)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for k in range(shape.K):
+        np.testing.assert_array_equal(dyd[p["dst_pos"][:, k]], want)
