@@ -378,6 +378,17 @@ def next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp):
     res["combine_backward"] = {"ms": round(ms, 4), "gbs": round(nb / ms / 1e6, 1),
                                "frac_of_peak": round(nb / ms / 1e6 / peak, 4), "bytes": nb}
     del dh, dy, dw
+    # inference budget: B = 1 slot per rank on the same routing, pieces beyond
+    # them read the home weights (mep_plan_remote_fallback)
+    pf = mep.mep_plan_remote_fallback(idx_d, s.R, s.S, s.K, s.E, 1)
+    ms = timed(lambda: mep.mep_plan_remote_fallback(idx_d, s.R, s.S, s.K, s.E, 1, out=pf))
+    cu = pf.cu_seqlens.cpu().numpy()
+    per = s.E // s.R
+    remote = sum(int((cu[r, :s.E] - np.concatenate([[0], cu[r, :s.E - 1]]) > 0).sum()) -
+                 int(((cu[r, :s.E] - np.concatenate([[0], cu[r, :s.E - 1]]))[r * per:(r + 1) * per] > 0).sum())
+                 for r in range(s.R))
+    res["plan_remote_fallback_B1"] = {"us": round(1000 * ms, 2), "remote_rows": remote,
+                                      "status": int(pf.status.item())}
     torch.cuda.synchronize()
     assert int(plan.status.item()) == 0
     res["note"] = "median of 20 reps after 3 warm-up, L2 flushed before each; same workload and plan"

@@ -132,6 +132,24 @@ MEP_API int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int B,
              int32_t* dst_pos, int32_t* status, void* stream);
 
 /*
+ * mep_plan_remote_fallback -- mep_plan under the inference reading of the
+ * slot budget ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库", 内存契约与权重
+ * 布局: inference may use B = 3-4; when a rank needs more remote experts than
+ * it has slots, their home rank's weights are read through the symmetric
+ * mapping, slower but correct). A rank's first B pieces, in pour order, take
+ * slots 0..B-1 as in mep_plan; every further piece of expert e takes row e
+ * (a [0, E) row, served by e's home weights) of the receiving rank, so a
+ * rank's non-home rows can be non-empty. MEP_ERR_CAPACITY never occurs.
+ * Arguments, outputs, workspace and the other errors are those of mep_plan;
+ * with enough slots the two plans are identical.
+ */
+MEP_API int mep_plan_remote_fallback(const int32_t* topk_idx, int R, int S, int K, int E, int B,
+                                     void* workspace, size_t workspace_bytes,
+                                     int32_t* expert_counts, int32_t* cu_seqlens,
+                                     int32_t* slot_expert, int32_t* dst_pos, int32_t* status,
+                                     void* stream);
+
+/*
  * mep_prefetch -- copy the planned redundant experts' weights into their
  * slots ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库", 核心技术: the
  * redundant experts' weights are prefetched before expert compute;

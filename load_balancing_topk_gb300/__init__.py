@@ -30,7 +30,7 @@ from typing import NamedTuple, Optional
 
 __all__ = [
     "MepError", "Plan", "library_path", "load_library", "status_string", "version",
-    "plan_workspace_bytes", "mep_plan", "mep_dispatch", "mep_combine", "mep_reduce_grad",
+    "plan_workspace_bytes", "mep_plan", "mep_plan_remote_fallback", "mep_dispatch", "mep_combine", "mep_reduce_grad",
     "mep_prefetch", "mep_dispatch_backward", "mep_combine_backward", "STATUS",
 ]
 
@@ -60,6 +60,7 @@ SIGNATURES = [
     ("mep_status_string", ctypes.c_char_p, [_I]),
     ("mep_plan_workspace_bytes", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     ("mep_plan", _I, [_VP, _I, _I, _I, _I, _I, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]),
+    ("mep_plan_remote_fallback", _I, [_VP, _I, _I, _I, _I, _I, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("mep_plan_static_scratch", _I, [_VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("mep_dispatch", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
     ("mep_combine", _I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
@@ -171,6 +172,17 @@ def mep_plan(topk_idx, R: int, S: int, K: int, E: int, B: int, out: Optional[Pla
 
     Nothing is synchronised: read ``status`` (0 = ok) when convenient.
     """
+    return _plan("mep_plan", topk_idx, R, S, K, E, B, out)
+
+
+def mep_plan_remote_fallback(topk_idx, R: int, S: int, K: int, E: int, B: int,
+                             out: Optional[Plan] = None) -> Plan:
+    """mep_plan under the inference reading: pieces beyond a rank's B slots
+    take the expert's own row (served by its home weights) instead of failing."""
+    return _plan("mep_plan_remote_fallback", topk_idx, R, S, K, E, B, out)
+
+
+def _plan(fn: str, topk_idx, R, S, K, E, B, out):
     torch = _torch()
     _need(topk_idx, "topk_idx", torch.int32, (R * S, K))
     dev = topk_idx.device
@@ -194,11 +206,11 @@ def mep_plan(topk_idx, R: int, S: int, K: int, E: int, B: int, out: Optional[Pla
         if out.workspace.numel() < ws_bytes:
             raise ValueError(f"workspace has {out.workspace.numel()} bytes, needs {ws_bytes}")
     with torch.cuda.device(dev):
-        rc = load_library().mep_plan(
+        rc = getattr(load_library(), fn)(
             _ptr(topk_idx), R, S, K, E, B, _ptr(out.workspace), out.workspace.numel(),
             _ptr(out.expert_counts), _ptr(out.cu_seqlens), _ptr(out.slot_expert),
             _ptr(out.dst_pos), _ptr(out.status), _stream(dev))
-    _check("mep_plan", rc)
+    _check(fn, rc)
     return out
 
 

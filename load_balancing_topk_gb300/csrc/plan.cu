@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kTileThreads)
 // k_plan: the single-CTA planner.
 struct PlanArgs {
   int nblk, R, S, K, E, B;
+  int fallback;          // pieces beyond B take the expert's own row instead of failing
   int32_t* counts;       // [E]
   int32_t* cu;           // [R, E+B]
   int32_t* slot_expert;  // [R, B]
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
         if (min(oe, hi) < oe) break;
       }
     }
-    if (np > B) s_cap = 1;
+    if (np > B && !a.fallback) s_cap = 1;
     sNp[r] = np;
     sQ0[r] = q0;
   }
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
       const int s = max(os, lo), en = min(oe, hi);
       const int g = sPex[r] + b;
       if (g >= E + R) break;  // cannot happen: pieces <= overflow experts + deficit ranks - 1
-      a.slot_expert[r * B + b] = e;
+      if (b < B) a.slot_expert[r * B + b] = e;
       a.ws.piece_lo[g] = sKeep[e] + (s - os);
       sPlen[g] = en - s;
       atomicMin(&sPcBeg[e], g);
@@ -380,23 +381,40 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
 
   // 5. cu_seqlens, one warp per rank; also the global first row of every
   //    home row and piece.
+  //    Pieces b < B sit in slot rows E + b; pieces b >= B (fallback only)
+  //    sit in the expert's own row e, found by a binary search over the
+  //    rank's remaining pieces, whose experts ascend with b.
   for (int r = warp; r < R; r += nwarps) {
     int carry = 0;
-    const int np = sNp[r], pex = sPex[r];
+    const int np = sNp[r], pex = sPex[r], q0 = sQ0[r];
+    const int nslot = min(np, B);
     for (int j0 = 0; j0 < G; j0 += 32) {
       const int j = j0 + lane;
-      int c = 0;
-      if (j < E) c = (j / per == r) ? sKeep[j] : 0;
-      else if (j - E < np) c = sPlen[pex + (j - E)];
+      int c = 0, g = -1;
+      if (j < E) {
+        if (j / per == r) {
+          c = sKeep[j];
+        } else if (np > B) {
+          int lo = B, hi = np;
+          while (lo < hi) {
+            const int m = (lo + hi) >> 1;
+            if (sOlist[q0 + m] < j) lo = m + 1; else hi = m;
+          }
+          if (lo < np && sOlist[q0 + lo] == j) {
+            g = pex + lo;
+            c = sPlen[g];
+          }
+        }
+      } else if (j < G && j - E < nslot) {
+        g = pex + (j - E);
+        c = sPlen[g];
+      }
       const int incl = warp_incl_scan(c);
       if (j < G) {
         a.cu[size_t(r) * G + j] = carry + incl;
         const int start = r * SK + carry + incl - c;
-        if (j < E) {
-          if (j / per == r) a.ws.home_base[j] = start;
-        } else if (j - E < np) {
-          a.ws.piece_base[pex + (j - E)] = start;
-        }
+        if (j < E && j / per == r) a.ws.home_base[j] = start;
+        else if (g >= 0) a.ws.piece_base[g] = start;
       }
       carry += __shfl_sync(MEP_FULL_MASK, incl, 31);
     }
@@ -528,10 +546,10 @@ extern "C" int mep_plan_workspace_bytes(int R, int S, int K, int E, int B, size_
   return MEP_OK;
 }
 
-extern "C" int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int B,
-                        void* workspace, size_t workspace_bytes, int32_t* expert_counts,
-                        int32_t* cu_seqlens, int32_t* slot_expert, int32_t* dst_pos,
-                        int32_t* status, void* stream) {
+static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int B, int fallback,
+                       void* workspace, size_t workspace_bytes, int32_t* expert_counts,
+                       int32_t* cu_seqlens, int32_t* slot_expert, int32_t* dst_pos,
+                       int32_t* status, void* stream) {
   int rc = plan_check(R, S, K, E, B);
   if (rc != MEP_OK) return rc;
   const int N = R * S;
@@ -558,7 +576,7 @@ extern "C" int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int
     return MEP_ERR_CUDA;
 
   if (nblk > 0) k_hist<<<nblk, kTileThreads, hist_smem, st>>>(topk_idx, N, K, E, tpt, ws);
-  PlanArgs pa{nblk, R, S, K, E, B, expert_counts, cu_seqlens, slot_expert, status, ws};
+  PlanArgs pa{nblk, R, S, K, E, B, fallback, expert_counts, cu_seqlens, slot_expert, status, ws};
   if (launch_pdl(k_plan, dim3(1), dim3(kPlanThreads), plan_smem, st, pa) != cudaSuccess)
     return MEP_ERR_CUDA;
   if (nblk > 0 &&
@@ -566,4 +584,21 @@ extern "C" int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int
                  tpt, nblk, ws, static_cast<const int32_t*>(status), dst_pos) != cudaSuccess)
     return MEP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
+}
+
+extern "C" int mep_plan(const int32_t* topk_idx, int R, int S, int K, int E, int B,
+                        void* workspace, size_t workspace_bytes, int32_t* expert_counts,
+                        int32_t* cu_seqlens, int32_t* slot_expert, int32_t* dst_pos,
+                        int32_t* status, void* stream) {
+  return plan_launch(topk_idx, R, S, K, E, B, 0, workspace, workspace_bytes, expert_counts,
+                     cu_seqlens, slot_expert, dst_pos, status, stream);
+}
+
+extern "C" int mep_plan_remote_fallback(const int32_t* topk_idx, int R, int S, int K, int E, int B,
+                                        void* workspace, size_t workspace_bytes,
+                                        int32_t* expert_counts, int32_t* cu_seqlens,
+                                        int32_t* slot_expert, int32_t* dst_pos, int32_t* status,
+                                        void* stream) {
+  return plan_launch(topk_idx, R, S, K, E, B, 1, workspace, workspace_bytes, expert_counts,
+                     cu_seqlens, slot_expert, dst_pos, status, stream);
 }

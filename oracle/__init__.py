@@ -72,6 +72,8 @@ def _load():
             lib.orc_counts.argtypes = [i32p, c_i64, ctypes.c_int, ctypes.c_int, i32p]
             lib.orc_plan.restype = ctypes.c_int
             lib.orc_plan.argtypes = [i32p] + [ctypes.c_int] * 5 + [i32p] * 7
+            lib.orc_plan_fallback.restype = ctypes.c_int
+            lib.orc_plan_fallback.argtypes = [i32p] + [ctypes.c_int] * 5 + [i32p] * 7
             lib.orc_dispatch.restype = None
             lib.orc_dispatch.argtypes = [ctypes.c_void_p, i32p, c_i64, ctypes.c_int, c_i64, ctypes.c_void_p]
             lib.orc_combine.restype = None
@@ -121,13 +123,16 @@ def counts(idx: np.ndarray, E: int) -> np.ndarray:
     return out
 
 
-def plan(idx: np.ndarray, R: int, S: int, K: int, E: int, B: int) -> dict:
+def plan(idx: np.ndarray, R: int, S: int, K: int, E: int, B: int, fallback: bool = False) -> dict:
     """Home-first plan of one layer's routing.
 
     Returns a dict with status ("ok" / "bad_routing" / "capacity" /
     "bad_arg"), counts [E], cu_seqlens [R, E+B] (inclusive ends),
     slot_expert [R, B] (-1 = unused), slot_lo / slot_len [R, B] (range of the
     expert's token list that the slot holds), dst_pos [R*S, K] and n_pieces.
+
+    fallback=True is the inference reading: a rank's pieces beyond B take the
+    expert's own row e of that rank instead of failing with "capacity".
     """
     idx = np.ascontiguousarray(idx, dtype=np.int32)
     N = R * S
@@ -143,7 +148,8 @@ def plan(idx: np.ndarray, R: int, S: int, K: int, E: int, B: int) -> dict:
         dst_pos=np.full((N, K), -1, dtype=np.int32),
     )
     npieces = np.zeros(1, dtype=np.int32)
-    st = _load().orc_plan(_i32(idx), R, S, K, E, B, _i32(out["counts"]), _i32(out["cu_seqlens"]),
+    fn = _load().orc_plan_fallback if fallback else _load().orc_plan
+    st = fn(_i32(idx), R, S, K, E, B, _i32(out["counts"]), _i32(out["cu_seqlens"]),
                           _i32(out["slot_expert"]), _i32(out["slot_lo"]), _i32(out["slot_len"]),
                           _i32(out["dst_pos"]), _i32(npieces))
     out["status"] = STATUS[st]

@@ -94,7 +94,7 @@ void orc_counts(const int32_t* idx, int64_t N, int K, int E, int32_t* counts) {
 typedef struct {
   int e;      /* expert */
   int r;      /* receiving rank */
-  int b;      /* slot on that rank */
+  int b;      /* slot on that rank; -1: the expert's own row e (fallback) */
   int64_t lo; /* first list index of e covered */
   int64_t hi; /* one past the last */
 } orc_piece;
@@ -106,10 +106,10 @@ typedef struct {
  * On ORC_BAD_ROUTING / ORC_CAPACITY: slot_expert = -1, cu = 0, slot_lo =
  * slot_len = 0, dst_pos untouched; counts hold T_e for the capacity case.
  */
-int orc_plan(const int32_t* idx, int R, int S, int K, int E, int B,
-             int32_t* counts, int32_t* cu, int32_t* slot_expert,
-             int32_t* slot_lo, int32_t* slot_len, int32_t* dst_pos,
-             int32_t* n_pieces_out) {
+static int plan_impl(const int32_t* idx, int R, int S, int K, int E, int B, int fallback,
+                     int32_t* counts, int32_t* cu, int32_t* slot_expert,
+                     int32_t* slot_lo, int32_t* slot_len, int32_t* dst_pos,
+                     int32_t* n_pieces_out) {
   const int64_t N = (int64_t)R * S;
   const int64_t A = N * K;
   const int64_t SK = (int64_t)S * K;
@@ -192,7 +192,9 @@ int orc_plan(const int32_t* idx, int R, int S, int K, int E, int B,
         avail = counts[oe] - opos;
         take = avail < need ? avail : need;
         b = nslot[r];
-        if (b >= B) {
+        if (b >= B && fallback) {
+          b = -1; /* no slot left: rank r reads expert oe's home weights (row oe) */
+        } else if (b >= B) {
           st = ORC_CAPACITY;
           goto fail;
         }
@@ -202,7 +204,7 @@ int orc_plan(const int32_t* idx, int R, int S, int K, int E, int B,
         pieces[npieces].lo = opos;
         pieces[npieces].hi = opos + take;
         ++npieces;
-        nslot[r] = b + 1;
+        if (b >= 0) nslot[r] = b + 1;
         opos += take;
         need -= take;
         if (opos == counts[oe]) {
@@ -218,6 +220,10 @@ int orc_plan(const int32_t* idx, int R, int S, int K, int E, int B,
   c = (int64_t*)calloc((size_t)R * (size_t)G, sizeof(int64_t));
   for (e = 0; e < E; ++e) c[(int64_t)(e / per) * G + e] = keep[e];
   for (j = 0; j < npieces; ++j) {
+    if (pieces[j].b < 0) { /* fallback piece: row e of the receiving rank */
+      c[(int64_t)pieces[j].r * G + pieces[j].e] = pieces[j].hi - pieces[j].lo;
+      continue;
+    }
     c[(int64_t)pieces[j].r * G + E + pieces[j].b] = pieces[j].hi - pieces[j].lo;
     slot_expert[pieces[j].r * B + pieces[j].b] = pieces[j].e;
     slot_lo[pieces[j].r * B + pieces[j].b] = (int32_t)pieces[j].lo;
@@ -246,7 +252,7 @@ int orc_plan(const int32_t* idx, int R, int S, int K, int E, int B,
         if (pieces[p].e == e && pieces[p].lo <= i && i < pieces[p].hi) found = p;
       /* found >= 0 always: the pieces of e cover [keep_e, T_e) */
       r = pieces[found].r;
-      j = E + pieces[found].b;
+      j = pieces[found].b >= 0 ? E + pieces[found].b : e;
       off = i - pieces[found].lo;
     }
     start = cu[(int64_t)r * G + j] - c[(int64_t)r * G + j];
@@ -273,6 +279,29 @@ done:
   free(fill);
   free(listpos);
   return st;
+}
+
+/* Training reading: more than B pieces on a rank is a capacity error. */
+int orc_plan(const int32_t* idx, int R, int S, int K, int E, int B,
+             int32_t* counts, int32_t* cu, int32_t* slot_expert,
+             int32_t* slot_lo, int32_t* slot_len, int32_t* dst_pos,
+             int32_t* n_pieces_out) {
+  return plan_impl(idx, R, S, K, E, B, 0, counts, cu, slot_expert, slot_lo, slot_len, dst_pos,
+                   n_pieces_out);
+}
+
+/* Inference reading ([umios] 内存契约与权重布局: inference may use B = 3-4;
+ * when more remote experts are needed, their home rank's weights are read
+ * through the symmetric mapping): a rank's pieces beyond its B slots are not
+ * an error; such a piece of expert e takes row e (a [0, E) row, served by the
+ * home weights) of the receiving rank. The first B pieces of a rank, in pour
+ * order, keep slots 0..B-1. */
+int orc_plan_fallback(const int32_t* idx, int R, int S, int K, int E, int B,
+                      int32_t* counts, int32_t* cu, int32_t* slot_expert,
+                      int32_t* slot_lo, int32_t* slot_len, int32_t* dst_pos,
+                      int32_t* n_pieces_out) {
+  return plan_impl(idx, R, S, K, E, B, 1, counts, cu, slot_expert, slot_lo, slot_len, dst_pos,
+                   n_pieces_out);
 }
 
 /* ------------------------------------------------------------------------ */
