@@ -44,24 +44,30 @@ def up_to_date(lib: str = LIB_PATH) -> bool:
 
 
 def build(force: bool = False, extra_flags: list[str] | None = None, lib: str = LIB_PATH,
-          verbose: bool = False) -> str:
-    """Compile csrc/*.cu and link ``libmep.so``; returns its path."""
-    if not force and extra_flags is None and up_to_date(lib):
+          verbose: bool = False, src_dir: str | None = None) -> str:
+    """Compile csrc/*.cu and link ``libmep.so``; returns its path.
+
+    extra_flags, lib and src_dir build a separate copy (other macros, another
+    output path, or a modified copy of csrc/) without touching the default
+    library."""
+    src = src_dir or CSRC
+    if not force and extra_flags is None and src_dir is None and up_to_date(lib):
         return lib
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-I" + INCLUDE, "-Xcompiler", "-fPIC",
                     "-Xcompiler", "-fvisibility=hidden"] + list(extra_flags or [])
-    tag = str(abs(hash(tuple(extra_flags or []))))[:8] if extra_flags else "main"
+    tag = (str(abs(hash((tuple(extra_flags or []), src))))[:8]
+           if (extra_flags or src_dir) else "main")
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, f"{os.path.splitext(src)[0]}.{tag}.o")
-        cmd = [cc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(name: str) -> str:
+        obj = os.path.join(BUILD_DIR, f"{os.path.splitext(name)[0]}.{tag}.o")
+        cmd = [cc] + flags + ["-I" + CSRC, "-c", os.path.join(src, name), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {name}:\n{r.stdout}\n{r.stderr}")
         return obj
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:

@@ -34,7 +34,10 @@ constexpr int kTileThreads = 256;            // k_hist / k_offsets block size (8
 constexpr int kTileWarps = kTileThreads / 32;
 constexpr int kTileAssign = 2048;            // assignments per tile (upper bound)
 constexpr int kWarpIters = kTileAssign / (32 * kTileWarps);  // 8 iterations per warp
-constexpr int kPlanThreads = 1024;           // k_plan block size
+#ifndef MEP_PLAN_THREADS
+#define MEP_PLAN_THREADS 1024
+#endif
+constexpr int kPlanThreads = MEP_PLAN_THREADS;  // k_plan block size
 constexpr int kMaxScanGroups = 64;           // tile groups in k_plan's prefix pass
 constexpr int kPartInts = 8192;              // k_plan shared ints for group sums
 
@@ -44,7 +47,7 @@ inline int tile_tokens(int K) { return (kTileAssign / K) & ~3; }
 
 struct PlanWs {
   int* blockhist;    // [nblk, E] tile counts
-  int* groupbase;    // [kMaxScanGroups, E] count of e in all tiles before the group
+  int* groupbase;    // [E, Gs] count of e in all tiles before group g (Gs <= kMaxScanGroups)
   int* blockerr;     // [nblk]
   int* keep;         // [E] tokens kept on the home row
   int* home_base;    // [E] global row of the home row's first token
@@ -182,7 +185,7 @@ template <> struct Vec<4> {
 // group that precede it, so no single CTA reads every tile count twice.
 // Columns are W experts wide; thread (g, c) owns group g of column c.
 __host__ __device__ inline void tile_groups(int nblk, int E, int* Gs, int* tpg) {
-  int g = kPartInts / E;
+  int g = kPartInts / E - 1;  // sPart holds E rows of Gs + 1 (padding) ints
   if (g > kMaxScanGroups) g = kMaxScanGroups;
   if (g > nblk) g = nblk;
   if (g < 1) g = 1;
@@ -211,18 +214,25 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT) {
       for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
     }
 #pragma unroll
-    for (int j = 0; j < W; ++j) sPart[g * E + c * W + j] = s[j];
+    for (int j = 0; j < W; ++j) sPart[(c * W + j) * (Gs + 1) + g] = s[j];
   }
   __syncthreads();
-  for (int e = tid; e < E; e += nthr) {
-    int run = 0;
-    for (int g = 0; g < Gs; ++g) {
-      const int v = sPart[g * E + e];
-      a.ws.groupbase[g * E + e] = run;
-      run += v;
+  // one warp per expert: exclusive scan over its Gs <= 64 group sums (rows
+  // padded to Gs + 1 ints: conflict-free), written as groupbase[e][g]
+  const int lane = tid & 31;
+  for (int e = tid >> 5; e < E; e += nthr >> 5) {
+    const int* row = sPart + e * (Gs + 1);
+    const int v0 = lane < Gs ? row[lane] : 0;
+    const int v1 = lane + 32 < Gs ? row[lane + 32] : 0;
+    const int i0 = warp_incl_scan(v0);
+    const int tot0 = __shfl_sync(MEP_FULL_MASK, i0, 31);
+    const int i1 = warp_incl_scan(v1);
+    if (lane < Gs) a.ws.groupbase[e * Gs + lane] = i0 - v0;
+    if (lane + 32 < Gs) a.ws.groupbase[e * Gs + lane + 32] = tot0 + i1 - v1;
+    if (lane == 31) {
+      sT[e] = tot0 + i1;
+      a.counts[e] = tot0 + i1;
     }
-    sT[e] = run;
-    a.counts[e] = run;
   }
   __syncthreads();
 }
@@ -295,26 +305,65 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   else tile_group_sums<1>(a, sPart, sT);
 
   // 2. home-first keep: the count of e's earlier home experts is a
-  //    difference of the running sum of T
-  block_excl_scan(sT, sPre, E, s_warp, true);
-  for (int e = tid; e < E; e += nthr) {
-    const int r = e / per;
-    const int before = sPre[e] - sPre[r * per];
-    const int kp = max(0, min(sT[e], SK - before));
-    sKeep[e] = kp;
-    sOv[e] = sT[e] - kp;
-    sFlag[e] = sOv[e] > 0 ? 1 : 0;
-    a.ws.keep[e] = kp;
+  //    difference of the running sum of T; then
+  // 3. overflow segments (expert order) and deficits (rank order) on one
+  //    line. Up to 1024 experts, warp 0 does both in one pass over chunks
+  //    of 32 experts (three warp scans per chunk, no block barrier);
+  //    beyond, block-wide scans.
+  if (E <= 1024) {
+    if (warp == 0) {
+      int cT = 0, cO = 0, cF = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const int T = e < E ? sT[e] : 0;
+        const int iT = warp_incl_scan(T);
+        if (e < E) sPre[e] = cT + iT - T;
+        cT += __shfl_sync(MEP_FULL_MASK, iT, 31);
+        __syncwarp();  // sPre of this chunk visible to the whole warp
+        int ov = 0;
+        if (e < E) {
+          const int r = e / per;
+          const int kp = max(0, min(T, SK - (sPre[e] - sPre[r * per])));
+          ov = T - kp;
+          sKeep[e] = kp;
+          sOv[e] = ov;
+          a.ws.keep[e] = kp;
+        }
+        const int iO = warp_incl_scan(ov);
+        if (e < E) sOst[e] = cO + iO - ov;
+        cO += __shfl_sync(MEP_FULL_MASK, iO, 31);
+        const int f = ov > 0 ? 1 : 0;
+        const int iF = warp_incl_scan(f);
+        if (f) sOlist[cF + iF - 1] = e;
+        cF += __shfl_sync(MEP_FULL_MASK, iF, 31);
+      }
+      if (lane == 0) {
+        sPre[E] = cT;
+        sOst[E] = cO;
+        sFlag[E] = cF;
+      }
+    }
+    __syncthreads();
+  } else {
+    block_excl_scan(sT, sPre, E, s_warp, true);
+    for (int e = tid; e < E; e += nthr) {
+      const int r = e / per;
+      const int before = sPre[e] - sPre[r * per];
+      const int kp = max(0, min(sT[e], SK - before));
+      sKeep[e] = kp;
+      sOv[e] = sT[e] - kp;
+      sFlag[e] = sOv[e] > 0 ? 1 : 0;
+      a.ws.keep[e] = kp;
+    }
+    __syncthreads();
+    block_excl_scan(sOv, sOst, E, s_warp, true);
+    block_excl_scan(sFlag, sFlag, E, s_warp, true);
+    for (int e = tid; e < E; e += nthr)
+      if (sOv[e] > 0) sOlist[sFlag[e]] = e;
   }
   for (int r = tid; r < R; r += nthr)
     sDef[r] = max(0, SK - (sPre[(r + 1) * per] - sPre[r * per]));
   __syncthreads();
-
-  // 3. overflow segments (expert order) and deficits (rank order) on one line
-  block_excl_scan(sOv, sOst, E, s_warp, true);
-  block_excl_scan(sFlag, sFlag, E, s_warp, true);
-  for (int e = tid; e < E; e += nthr)
-    if (sOv[e] > 0) sOlist[sFlag[e]] = e;
   warp0_excl_scan(sDef, sDst, R);
   const int nov = sFlag[E];
 
@@ -429,14 +478,18 @@ __global__ void __launch_bounds__(kTileThreads)
               int nblk, PlanWs ws, const int32_t* __restrict__ status,
               int32_t* __restrict__ dst_pos) {
   extern __shared__ int smem[];
-  int* s_idx = smem;                    // [kTileAssign]
-  int* s_wcnt = smem + kTileAssign;     // [kTileWarps, E]
+  int* s_idx = smem;                          // [kTileAssign]
+  int* s_wcnt = smem + kTileAssign;           // [kTileWarps, E]
+  int* s_keep = s_wcnt + kTileWarps * E;      // [E]
+  int* s_hb = s_keep + E;                     // [E]
   const int blk = blockIdx.x;
   const int t0 = blk * tok_per_tile;
   const int ntok = min(tok_per_tile, N - t0);
   const int na = ntok * K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // the tile's routing does not depend on the planner: stage it first
+  // Everything up to the wait depends only on this tile's routing, so it
+  // overlaps the planner: stage the tile, then rank each assignment among
+  // the tile's assignments of the same expert.
   {
     const int32_t* g = topk_idx + size_t(t0) * K;
     const int nv = na >> 2;
@@ -446,13 +499,12 @@ __global__ void __launch_bounds__(kTileThreads)
     for (int i = (nv << 2) + threadIdx.x; i < na; i += blockDim.x) s_idx[i] = __ldg(g + i);
   }
   for (int i = threadIdx.x; i < kTileWarps * E; i += blockDim.x) s_wcnt[i] = 0;
-  pdl_wait();                           // the planner's tables and status
-  pdl_launch_dependents();
-  if (read_status(status) != 0) return;
   __syncthreads();
 
   // Warp w owns the contiguous assignment range [wbeg, wend) of the tile,
   // so (warp, iteration, lane) order is the flattened (token, k) order.
+  // Ids outside [0, E) are skipped here; the planner then reports bad
+  // routing and the kernel returns after the wait without writing.
   const int chunk = (((na + kTileWarps - 1) / kTileWarps) + 31) & ~31;
   const int wbeg = min(na, warp * chunk), wend = min(na, wbeg + chunk);
   int* wc = s_wcnt + warp * E;
@@ -462,8 +514,8 @@ __global__ void __launch_bounds__(kTileThreads)
     loc[j] = 0;
     const int a = wbeg + j * 32 + lane;
     if (wbeg + j * 32 < wend) {          // warp-uniform
-      const bool in = a < wend;
-      const int e = in ? s_idx[a] : -1;
+      const int e = a < wend ? s_idx[a] : -1;
+      const bool in = e >= 0 && e < E;
       const unsigned m = __ballot_sync(MEP_FULL_MASK, in);
       int cur = 0;
       unsigned peers = 0;
@@ -478,15 +530,21 @@ __global__ void __launch_bounds__(kTileThreads)
     }
   }
   __syncthreads();
-  // per expert: exclusive prefix over warps, on top of the tile's prefix
-  // (the group's base plus the group's earlier tiles)
+
+  pdl_wait();                           // the planner's tables and status
+  pdl_launch_dependents();
+  const int st = status != nullptr ? __ldcg(status) : 0;
+  // per expert: the tile's prefix (the group's base plus the group's earlier
+  // tiles) and the planner's tables, all loads issued together
   int Gs, tpg;
   tile_groups(nblk, E, &Gs, &tpg);
   const int g = blk / tpg;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = ws.groupbase[g * E + e];
+    int run = __ldcg(ws.groupbase + e * Gs + g);
+    s_keep[e] = __ldcg(ws.keep + e);
+    s_hb[e] = __ldcg(ws.home_base + e);
 #pragma unroll 4
-    for (int b = g * tpg; b < blk; ++b) run += ws.blockhist[size_t(b) * E + e];
+    for (int b = g * tpg; b < blk; ++b) run += __ldcg(ws.blockhist + size_t(b) * E + e);
 #pragma unroll
     for (int w = 0; w < kTileWarps; ++w) {
       const int v = s_wcnt[w * E + e];
@@ -494,6 +552,7 @@ __global__ void __launch_bounds__(kTileThreads)
       run += v;
     }
   }
+  if (st != 0) return;                  // uniform: one status word
   __syncthreads();
   int32_t* out = dst_pos + size_t(t0) * K;
 #pragma unroll
@@ -502,16 +561,15 @@ __global__ void __launch_bounds__(kTileThreads)
     if (a < wend) {
       const int e = s_idx[a];
       const int i = wc[e] + loc[j];     // index of the token in expert e's list
-      const int kp = __ldg(ws.keep + e);
       int row;
-      if (i < kp) {
-        row = __ldg(ws.home_base + e) + i;
+      if (i < s_keep[e]) {
+        row = s_hb[e] + i;
       } else {
-        const int p0 = __ldg(ws.pc_begin + e), pn = __ldg(ws.pc_count + e);
+        const int p0 = __ldcg(ws.pc_begin + e), pn = __ldcg(ws.pc_count + e);
         int p = p0;
         for (int q = p0 + 1; q < p0 + pn; ++q)
-          if (__ldg(ws.piece_lo + q) <= i) p = q;
-        row = __ldg(ws.piece_base + p) + (i - __ldg(ws.piece_lo + p));
+          if (__ldcg(ws.piece_lo + q) <= i) p = q;
+        row = __ldcg(ws.piece_base + p) + (i - __ldcg(ws.piece_lo + p));
       }
       out[a] = row;
     }
@@ -567,7 +625,7 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
   const int tpt = tile_tokens(K);
 
   const int hist_smem = E * int(sizeof(int));
-  const int offs_smem = (kTileAssign + kTileWarps * E) * int(sizeof(int));
+  const int offs_smem = (kTileAssign + (kTileWarps + 2) * E) * int(sizeof(int));
   const int npart = kPartInts;
   const int plan_smem = int(sizeof(int)) * (9 * (E + 1) + (E + R) + npart + 5 * (R + 1));
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_hist), hist_smem) ||

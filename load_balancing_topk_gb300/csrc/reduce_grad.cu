@@ -24,7 +24,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVecPerThread = 4;  // float4 vectors per thread per item
-constexpr int kSlotBatch = 4;     // slot vectors loaded together
+#ifndef MEP_REDUCE_SLOT_BATCH
+#define MEP_REDUCE_SLOT_BATCH 4
+#endif
+constexpr int kSlotBatch = MEP_REDUCE_SLOT_BATCH;  // slot vectors loaded together
 
 __device__ __forceinline__ void add4(float4& a, const float4& b) {
   a.x = __fadd_rn(a.x, b.x);
