@@ -14,8 +14,9 @@
 //   cp.async.bulk and wrote them back with K bulk stores per row measured
 //   4-8% slower on GB300, at 4 KB and at 14 KB rows.)
 // combine: one warp per token; each lane owns 16-byte column vectors and
-//   issues the K gathers of a vector before its fp32 fused multiply-add
-//   chain (k in order), then writes the bf16 result (nearest-even).
+//   issues the K gathers of two vectors before their fp32 fused
+//   multiply-add chains (k in order), then writes the bf16 results
+//   (nearest-even).
 
 #include <cuda_bf16.h>
 
@@ -38,6 +39,10 @@ namespace mep {
 namespace {
 
 constexpr int kUnroll = MEP_DISPATCH_UNROLL;
+#ifndef MEP_COMBINE_UNROLL
+#define MEP_COMBINE_UNROLL 2
+#endif
+constexpr int kCombineUnroll = MEP_COMBINE_UNROLL;  // column vectors per lane in flight
 
 // One warp per token (grid-stride). Each lane holds kUnroll 16-byte vectors
 // of the row and writes each to the K destination rows with streaming
@@ -171,14 +176,22 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
         rows[k] = (long long)__shfl_sync(MEP_FULL_MASK, r0, k) * vpr;
         ws[k] = __shfl_sync(MEP_FULL_MASK, w0, k);
       }
-      for (long long v = lane; v < vpr; v += 32) {
-        uint4 q[KT];
+      for (long long v0 = lane; v0 < vpr; v0 += 32 * kCombineUnroll) {
+        uint4 q[kCombineUnroll][KT];
 #pragma unroll
-        for (int k = 0; k < KT; ++k) q[k] = __ldg(y + rows[k] + v);
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int u = 0; u < kCombineUnroll; ++u)
+          if (v0 + 32 * u < vpr) {
 #pragma unroll
-        for (int k = 0; k < KT; ++k) fma8(acc, ws[k], q[k]);
-        o[v] = pack8(acc);
+            for (int k = 0; k < KT; ++k) q[u][k] = __ldg(y + rows[k] + v0 + 32 * u);
+          }
+#pragma unroll
+        for (int u = 0; u < kCombineUnroll; ++u)
+          if (v0 + 32 * u < vpr) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < KT; ++k) fma8(acc, ws[k], q[u][k]);
+            o[v0 + 32 * u] = pack8(acc);
+          }
       }
     } else {
       for (long long v = lane; v < vpr; v += 32) {

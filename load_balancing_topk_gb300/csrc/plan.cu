@@ -40,6 +40,9 @@ constexpr int kWarpIters = kTileAssign / (32 * kTileWarps);  // 8 iterations per
 constexpr int kPlanThreads = MEP_PLAN_THREADS;  // k_plan block size
 constexpr int kMaxScanGroups = 64;           // tile groups in k_plan's prefix pass
 constexpr int kPartInts = 8192;              // k_plan shared ints for group sums
+#ifndef MEP_PLAN_WARP_SCAN_MAX_E
+#define MEP_PLAN_WARP_SCAN_MAX_E 128
+#endif
 
 // tokens per tile: as many as fit 2048 assignments, a multiple of 4 so that
 // every tile starts on a 16-byte boundary of topk_idx.
@@ -184,10 +187,17 @@ template <> struct Vec<4> {
 // before g (groupbase). Each k_offsets CTA adds the few tiles of its own
 // group that precede it, so no single CTA reads every tile count twice.
 // Columns are W experts wide; thread (g, c) owns group g of column c.
+// Row pitch of the shared group sums: odd, so that the column writes of
+// tile_group_sums spread over 8 banks; a single group needs no padding.
+__host__ __device__ inline int part_pitch(int Gs) {
+  return Gs == 1 ? 1 : ((Gs & 1) ? Gs + 2 : Gs + 1);
+}
+
+// The most groups (<= kMaxScanGroups, <= nblk) whose E rows of part_pitch
+// ints fit kPartInts; E <= MEP_MAX_E = kPartInts / 2 always fits one group.
 __host__ __device__ inline void tile_groups(int nblk, int E, int* Gs, int* tpg) {
-  int g = kPartInts / E - 1;  // sPart holds E rows of Gs + 1 (padding) ints
-  if (g > kMaxScanGroups) g = kMaxScanGroups;
-  if (g > nblk) g = nblk;
+  int g = nblk < kMaxScanGroups ? nblk : kMaxScanGroups;
+  while (g > 1 && E * part_pitch(g) > kPartInts) --g;
   if (g < 1) g = 1;
   *Gs = g;
   *tpg = nblk > 0 ? (nblk + g - 1) / g : 1;
@@ -200,6 +210,7 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT) {
   const int nc = E / W;
   int Gs, tpg;
   tile_groups(nblk, E, &Gs, &tpg);
+  const int P = part_pitch(Gs);
   const V* h = reinterpret_cast<const V*>(a.ws.blockhist);
   for (int x = tid; x < Gs * nc; x += nthr) {
     const int g = x / nc, c = x - g * nc;
@@ -214,14 +225,15 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT) {
       for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
     }
 #pragma unroll
-    for (int j = 0; j < W; ++j) sPart[(c * W + j) * (Gs + 1) + g] = s[j];
+    for (int j = 0; j < W; ++j) sPart[(c * W + j) * P + g] = s[j];
   }
   __syncthreads();
   // one warp per expert: exclusive scan over its Gs <= 64 group sums (rows
-  // padded to Gs + 1 ints: conflict-free), written as groupbase[e][g]
+  // of odd pitch P: the column writes above hit 8 banks, the row reads
+  // below are conflict-free), written as groupbase[e][g]
   const int lane = tid & 31;
   for (int e = tid >> 5; e < E; e += nthr >> 5) {
-    const int* row = sPart + e * (Gs + 1);
+    const int* row = sPart + e * P;
     const int v0 = lane < Gs ? row[lane] : 0;
     const int v1 = lane + 32 < Gs ? row[lane + 32] : 0;
     const int i0 = warp_incl_scan(v0);
@@ -307,10 +319,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   // 2. home-first keep: the count of e's earlier home experts is a
   //    difference of the running sum of T; then
   // 3. overflow segments (expert order) and deficits (rank order) on one
-  //    line. Up to 1024 experts, warp 0 does both in one pass over chunks
+  //    line. Up to 128 experts, warp 0 does both in one pass over chunks
   //    of 32 experts (three warp scans per chunk, no block barrier);
-  //    beyond, block-wide scans.
-  if (E <= 1024) {
+  //    beyond, block-wide scans (faster on GB300 from E = 256 on).
+  if (E <= MEP_PLAN_WARP_SCAN_MAX_E) {
     if (warp == 0) {
       int cT = 0, cO = 0, cF = 0;
       for (int e0 = 0; e0 < E; e0 += 32) {
@@ -474,14 +486,19 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
 // ---------------------------------------------------------------------------
 // k_offsets: destination rows.
 __global__ void __launch_bounds__(kTileThreads)
-    k_offsets(const int32_t* __restrict__ topk_idx, int N, int K, int E, int tok_per_tile,
-              int nblk, PlanWs ws, const int32_t* __restrict__ status,
-              int32_t* __restrict__ dst_pos) {
+    k_offsets(const int32_t* __restrict__ topk_idx, int N, int K, int E, int R,
+              int tok_per_tile, int nblk, int pieces_smem, PlanWs ws,
+              const int32_t* __restrict__ status, int32_t* __restrict__ dst_pos) {
   extern __shared__ int smem[];
   int* s_idx = smem;                          // [kTileAssign]
   int* s_wcnt = smem + kTileAssign;           // [kTileWarps, E]
   int* s_keep = s_wcnt + kTileWarps * E;      // [E]
   int* s_hb = s_keep + E;                     // [E]
+  int* s_pcb = s_hb + E;                      // [E] first piece of the expert
+  int* s_pcn = s_pcb + E;                     // [E] pieces of the expert
+  // piece tables: in shared memory when they fit (pieces_smem), else global
+  const int* s_plo = pieces_smem ? s_pcn + E : ws.piece_lo;          // [E+R]
+  const int* s_pbase = pieces_smem ? s_pcn + 2 * E + R : ws.piece_base;  // [E+R]
   const int blk = blockIdx.x;
   const int t0 = blk * tok_per_tile;
   const int ntok = min(tok_per_tile, N - t0);
@@ -543,6 +560,8 @@ __global__ void __launch_bounds__(kTileThreads)
     int run = __ldcg(ws.groupbase + e * Gs + g);
     s_keep[e] = __ldcg(ws.keep + e);
     s_hb[e] = __ldcg(ws.home_base + e);
+    s_pcb[e] = __ldcg(ws.pc_begin + e);
+    s_pcn[e] = __ldcg(ws.pc_count + e);
 #pragma unroll 4
     for (int b = g * tpg; b < blk; ++b) run += __ldcg(ws.blockhist + size_t(b) * E + e);
 #pragma unroll
@@ -552,6 +571,11 @@ __global__ void __launch_bounds__(kTileThreads)
       run += v;
     }
   }
+  if (pieces_smem)
+    for (int q = threadIdx.x; q < E + R; q += blockDim.x) {
+      s_pcn[E + q] = __ldcg(ws.piece_lo + q);
+      s_pcn[2 * E + R + q] = __ldcg(ws.piece_base + q);
+    }
   if (st != 0) return;                  // uniform: one status word
   __syncthreads();
   int32_t* out = dst_pos + size_t(t0) * K;
@@ -565,11 +589,11 @@ __global__ void __launch_bounds__(kTileThreads)
       if (i < s_keep[e]) {
         row = s_hb[e] + i;
       } else {
-        const int p0 = __ldcg(ws.pc_begin + e), pn = __ldcg(ws.pc_count + e);
+        const int p0 = s_pcb[e], pn = s_pcn[e];
         int p = p0;
         for (int q = p0 + 1; q < p0 + pn; ++q)
-          if (__ldcg(ws.piece_lo + q) <= i) p = q;
-        row = __ldcg(ws.piece_base + p) + (i - __ldcg(ws.piece_lo + p));
+          if (s_plo[q] <= i) p = q;
+        row = s_pbase[p] + (i - s_plo[p]);
       }
       out[a] = row;
     }
@@ -625,7 +649,12 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
   const int tpt = tile_tokens(K);
 
   const int hist_smem = E * int(sizeof(int));
-  const int offs_smem = (kTileAssign + (kTileWarps + 2) * E) * int(sizeof(int));
+  // k_offsets keeps its tile, per-warp counters and per-expert tables in
+  // shared memory, and the piece tables too when all of it fits
+  const int offs_base = (kTileAssign + (kTileWarps + 4) * E) * int(sizeof(int));
+  const int offs_pieces = 2 * (E + R) * int(sizeof(int));
+  const int pieces_smem = offs_base + offs_pieces <= 220 * 1024 ? 1 : 0;
+  const int offs_smem = offs_base + (pieces_smem ? offs_pieces : 0);
   const int npart = kPartInts;
   const int plan_smem = int(sizeof(int)) * (9 * (E + 1) + (E + R) + npart + 5 * (R + 1));
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_hist), hist_smem) ||
@@ -638,8 +667,9 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
   if (launch_pdl(k_plan, dim3(1), dim3(kPlanThreads), plan_smem, st, pa) != cudaSuccess)
     return MEP_ERR_CUDA;
   if (nblk > 0 &&
-      launch_pdl(k_offsets, dim3(nblk), dim3(kTileThreads), offs_smem, st, topk_idx, N, K, E,
-                 tpt, nblk, ws, static_cast<const int32_t*>(status), dst_pos) != cudaSuccess)
+      launch_pdl(k_offsets, dim3(nblk), dim3(kTileThreads), offs_smem, st, topk_idx, N, K, E, R,
+                 tpt, nblk, pieces_smem, ws, static_cast<const int32_t*>(status),
+                 dst_pos) != cudaSuccess)
     return MEP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
