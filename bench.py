@@ -275,33 +275,55 @@ def gpu_arm(args, rank: int, world: int, dist):
     nxt = next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp) if rank == 0 else None
 
     # --- end to end through the public API with host buffers -------------
+    # Every step copies its inputs (topk_idx, topk_w, hidden) from pinned host
+    # memory and its result (out, status) back, inside the timed region. The
+    # copies run on their own streams, double-buffered, so step i+1's inputs
+    # and step i-1's result move while step i computes.
     idx_h = torch.from_numpy(idx).pin_memory()
     w_h = torch.from_numpy(w).pin_memory()
     x_h = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
-    out_h = torch.empty((s.N, s.H), dtype=torch.bfloat16).pin_memory()
-    st_h = torch.empty(1, dtype=torch.int32).pin_memory()
-    idx_e = torch.empty_like(idx_d)
-    w_e = torch.empty_like(w_d)
-    x_e = torch.empty_like(x_d)
-    e2e_ms = []
-    e2e_steps = max(3, min(args.steps, 50))
-    for i in range(e2e_steps + 2):
-        untimed_reset()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        idx_e.copy_(idx_h, non_blocking=True)
-        w_e.copy_(w_h, non_blocking=True)
-        x_e.copy_(x_h, non_blocking=True)
-        p2 = mep.mep_plan(idx_e, s.R, s.S, s.K, s.E, s.B, out=plan)
-        mep.mep_dispatch(x_e, p2.dst_pos, p2.status, s.R, s.S, s.K, buf=buf)
-        mep.mep_combine(buf, w_e, p2.dst_pos, p2.status, s.R, s.S, s.K, out=out)
-        mep.mep_reduce_grad(p2.slot_expert, home_d, slots_d, p2.status, s.E)
-        out_h.copy_(out, non_blocking=True)
-        st_h.copy_(p2.status, non_blocking=True)
-        b.record()
-        b.synchronize()
-        if i >= 2:
-            e2e_ms.append(a.elapsed_time(b))
+    sets = [dict(idx=torch.empty_like(idx_d), w=torch.empty_like(w_d), x=torch.empty_like(x_d),
+                 out=torch.empty_like(out),
+                 out_h=torch.empty((s.N, s.H), dtype=torch.bfloat16).pin_memory(),
+                 st_h=torch.empty(1, dtype=torch.int32).pin_memory()) for _ in range(2)]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def e2e_run(nsteps):
+        ev = [[torch.cuda.Event() for _ in range(3)] for _ in range(nsteps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(s_in)
+        for i in range(nsteps):
+            b = sets[i % 2]
+            if i >= 2:
+                s_in.wait_event(ev[i - 2][1])       # step i-2 has read this input set
+            with torch.cuda.stream(s_in):
+                b["idx"].copy_(idx_h, non_blocking=True)
+                b["w"].copy_(w_h, non_blocking=True)
+                b["x"].copy_(x_h, non_blocking=True)
+                ev[i][0].record(s_in)
+            s_cmp.wait_event(ev[i][0])
+            if i >= 2:
+                s_cmp.wait_event(ev[i - 2][2])      # step i-2's result has left this out buffer
+            with torch.cuda.stream(s_cmp):
+                p2 = mep.mep_plan(b["idx"], s.R, s.S, s.K, s.E, s.B, out=plan)
+                mep.mep_dispatch(b["x"], p2.dst_pos, p2.status, s.R, s.S, s.K, buf=buf)
+                mep.mep_combine(buf, b["w"], p2.dst_pos, p2.status, s.R, s.S, s.K, out=b["out"])
+                mep.mep_reduce_grad(p2.slot_expert, home_d, slots_d, p2.status, s.E)
+                b["st_h"].copy_(p2.status, non_blocking=True)
+                ev[i][1].record(s_cmp)
+            s_out.wait_event(ev[i][1])
+            with torch.cuda.stream(s_out):
+                b["out_h"].copy_(b["out"], non_blocking=True)
+                ev[i][2].record(s_out)
+        t1.record(s_out)
+        t1.synchronize()
+        return t0.elapsed_time(t1)
+
+    e2e_run(max(3, args.warmup))
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_ms = [e2e_run(e2e_steps) / e2e_steps]
+    assert all(int(b["st_h"].item()) == 0 for b in sets)
     h2d = idx.nbytes + w.nbytes + x_np.nbytes
     d2h = s.N * s.H * 2 + 4
 
@@ -644,8 +666,9 @@ def main():
         "e2e": {"value": round(whole_job_gbs(world, res["total_bytes"], res["e2e_ms"]), 1),
                 "unit": "GB/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "ms_per_step": round(res["e2e_ms"], 4),
-                "note": "pinned host topk_idx/topk_w/hidden -> device, full step, out+status -> host; "
-                        "gradient tensors stay device-resident"},
+                "note": "every step: pinned host topk_idx/topk_w/hidden -> device, full step, "
+                        "out+status -> host; copies on their own streams, double-buffered, overlapping "
+                        "the neighbouring steps' compute; gradient tensors stay device-resident"},
         "gpu_launches": 6 * K,
         "clocks": res["clocks"],
         "cpu_baseline": cpu,

@@ -7,10 +7,11 @@
 // back; the shapes are static so no host sync is needed).
 //
 // dispatch: each token row is read from HBM once and written K times. One
-//   warp per token: every lane loads 4 coalesced 16-byte vectors of the row
-//   and stores each to the K destination rows with streaming stores; 16
-//   CTAs of 8 warps per SM keep enough stores in flight to run at the HBM
-//   write rate. (A design that staged rows in shared memory with
+//   warp per token: every lane loads 8 coalesced 32-byte vectors of the row
+//   (16-byte ones when H % 16 != 0 or a pointer is not 32-byte aligned) and
+//   stores each to the K destination rows with streaming stores; 16 CTAs
+//   of 8 warps per SM keep enough stores in flight to run at the HBM write
+//   rate. (A design that staged rows in shared memory with
 //   cp.async.bulk and wrote them back with K bulk stores per row measured
 //   4-8% slower on GB300, at 4 KB and at 14 KB rows.)
 // combine: one warp per token; each lane owns 16-byte column vectors and
@@ -26,7 +27,10 @@
 #define MEP_DISPATCH_WARPS 8
 #endif
 #ifndef MEP_DISPATCH_UNROLL
-#define MEP_DISPATCH_UNROLL 4
+#define MEP_DISPATCH_UNROLL 8
+#endif
+#ifndef MEP_DISPATCH_V32
+#define MEP_DISPATCH_V32 1
 #endif
 #ifndef MEP_DISPATCH_CTAS_PER_SM
 #define MEP_DISPATCH_CTAS_PER_SM 16
@@ -44,17 +48,45 @@ constexpr int kUnroll = MEP_DISPATCH_UNROLL;
 #endif
 constexpr int kCombineUnroll = MEP_COMBINE_UNROLL;  // column vectors per lane in flight
 
-// One warp per token (grid-stride). Each lane holds kUnroll 16-byte vectors
+// 16- and 32-byte vectors. The 32-byte forms (ld/st .v8.b32, sm_100 and
+// later) halve the memory instructions per byte; they need 32-byte aligned
+// addresses, which the host guarantees before choosing them.
+struct alignas(32) Vec32 {
+  uint32_t w[8];
+};
+
+__device__ __forceinline__ uint4 ld_nc(const uint4* p) { return __ldg(p); }
+__device__ __forceinline__ void st_cs(uint4* p, const uint4& v) { __stcs(p, v); }
+
+__device__ __forceinline__ Vec32 ld_nc(const Vec32* p) {
+  Vec32 v;
+  asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+        "=r"(v.w[6]), "=r"(v.w[7])
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_cs(Vec32* p, const Vec32& v) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+               "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]),
+               "r"(v.w[6]), "r"(v.w[7])
+               : "memory");
+}
+
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+// One warp per token (grid-stride). Each lane holds kUnroll vectors
 // of the row and writes each to the K destination rows with streaming
 // (evict-first) stores: the buffer is written once here and read back by the
 // expert computation, not by this kernel. KT > 0: K fixed at compile time,
 // destination offsets held in registers; KT == 0: any K, offsets re-read
 // per vector (L1 hits).
-template <int KT>
+template <int KT, typename V>
 __global__ void __launch_bounds__(32 * MEP_DISPATCH_WARPS)
-    k_dispatch(const uint4* __restrict__ hidden, const int32_t* __restrict__ dst_pos,
+    k_dispatch(const V* __restrict__ hidden, const int32_t* __restrict__ dst_pos,
                int32_t* status, long long N, int Kr, long long vpr, long long nrows,
-               uint4* __restrict__ buf) {
+               V* __restrict__ buf) {
   pdl_wait();
   pdl_launch_dependents();
   if (read_status(status) != 0) return;
@@ -68,7 +100,7 @@ __global__ void __launch_bounds__(32 * MEP_DISPATCH_WARPS)
     const bool bad = (lane < K && (r0 < 0 || r0 >= nrows)) ||
                      (lane + 32 < K && (r1 < 0 || r1 >= nrows));
     if (__any_sync(MEP_FULL_MASK, bad) && lane == 0) set_status(status, MEP_ERR_BAD_POSITION);
-    const uint4* src = hidden + t * vpr;
+    const V* src = hidden + t * vpr;
     if constexpr (KT > 0) {
       long long off[KT];
 #pragma unroll
@@ -77,32 +109,32 @@ __global__ void __launch_bounds__(32 * MEP_DISPATCH_WARPS)
         off[k] = (r >= 0 && r < nrows) ? (long long)r * vpr : -1;
       }
       for (long long v0 = lane; v0 < vpr; v0 += 32 * kUnroll) {
-        uint4 q[kUnroll];
+        V q[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-          if (v0 + 32 * u < vpr) q[u] = __ldg(src + v0 + 32 * u);
+          if (v0 + 32 * u < vpr) q[u] = ld_nc(src + v0 + 32 * u);
 #pragma unroll
         for (int k = 0; k < KT; ++k) {
           if (off[k] < 0) continue;
-          uint4* o = buf + off[k] + v0;
+          V* o = buf + off[k] + v0;
 #pragma unroll
           for (int u = 0; u < kUnroll; ++u)
-            if (v0 + 32 * u < vpr) __stcs(o + 32 * u, q[u]);
+            if (v0 + 32 * u < vpr) st_cs(o + 32 * u, q[u]);
         }
       }
     } else {
       for (long long v0 = lane; v0 < vpr; v0 += 32 * kUnroll) {
-        uint4 q[kUnroll];
+        V q[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u)
-          if (v0 + 32 * u < vpr) q[u] = __ldg(src + v0 + 32 * u);
+          if (v0 + 32 * u < vpr) q[u] = ld_nc(src + v0 + 32 * u);
         for (int k = 0; k < K; ++k) {
           const int r = __ldg(dst_pos + t * K + k);
           if (r < 0 || r >= nrows) continue;
-          uint4* o = buf + (long long)r * vpr + v0;
+          V* o = buf + (long long)r * vpr + v0;
 #pragma unroll
           for (int u = 0; u < kUnroll; ++u)
-            if (v0 + 32 * u < vpr) __stcs(o + 32 * u, q[u]);
+            if (v0 + 32 * u < vpr) st_cs(o + 32 * u, q[u]);
         }
       }
     }
@@ -110,13 +142,18 @@ __global__ void __launch_bounds__(32 * MEP_DISPATCH_WARPS)
 }
 
 template <int KT>
-cudaError_t launch_dispatch(const uint4* x, const int32_t* dst, int32_t* status, long long N,
-                            int K, long long vpr, long long nrows, uint4* buf, cudaStream_t st) {
+cudaError_t launch_dispatch(const void* x, const int32_t* dst, int32_t* status, long long N,
+                            int K, int H, long long nrows, void* buf, cudaStream_t st) {
   const long long want = (N + MEP_DISPATCH_WARPS - 1) / MEP_DISPATCH_WARPS;
   const long long cap = (long long)sm_count() * MEP_DISPATCH_CTAS_PER_SM;
   const int grid = int(want < cap ? want : cap);
-  return launch_pdl(k_dispatch<KT>, dim3(grid), dim3(32 * MEP_DISPATCH_WARPS), 0, st, x, dst,
-                    status, N, K, vpr, nrows, buf);
+  if (MEP_DISPATCH_V32 && H % 16 == 0 && aligned32(x) && aligned32(buf))
+    return launch_pdl(k_dispatch<KT, Vec32>, dim3(grid), dim3(32 * MEP_DISPATCH_WARPS), 0, st,
+                      static_cast<const Vec32*>(x), dst, status, N, K, (long long)(H / 16), nrows,
+                      static_cast<Vec32*>(buf));
+  return launch_pdl(k_dispatch<KT, uint4>, dim3(grid), dim3(32 * MEP_DISPATCH_WARPS), 0, st,
+                    static_cast<const uint4*>(x), dst, status, N, K, (long long)(H / 8), nrows,
+                    static_cast<uint4*>(buf));
 }
 
 // ---------------------------------------------------------------------------
@@ -365,19 +402,16 @@ extern "C" int mep_dispatch(const mep_bf16* hidden, const int32_t* dst_pos, int3
   if (rc != MEP_OK) return rc;
   const long long N = (long long)R * S;
   if (N == 0) return MEP_OK;
-  const long long vpr = H / 8;
-  const uint4* x4 = reinterpret_cast<const uint4*>(hidden);
-  uint4* b4 = reinterpret_cast<uint4*>(buf);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long long nrows = N * K;
   cudaError_t err;
   switch (K) {
-    case 1: err = launch_dispatch<1>(x4, dst_pos, status, N, K, vpr, nrows, b4, st); break;
-    case 2: err = launch_dispatch<2>(x4, dst_pos, status, N, K, vpr, nrows, b4, st); break;
-    case 4: err = launch_dispatch<4>(x4, dst_pos, status, N, K, vpr, nrows, b4, st); break;
-    case 6: err = launch_dispatch<6>(x4, dst_pos, status, N, K, vpr, nrows, b4, st); break;
-    case 8: err = launch_dispatch<8>(x4, dst_pos, status, N, K, vpr, nrows, b4, st); break;
-    default: err = launch_dispatch<0>(x4, dst_pos, status, N, K, vpr, nrows, b4, st); break;
+    case 1: err = launch_dispatch<1>(hidden, dst_pos, status, N, K, H, nrows, buf, st); break;
+    case 2: err = launch_dispatch<2>(hidden, dst_pos, status, N, K, H, nrows, buf, st); break;
+    case 4: err = launch_dispatch<4>(hidden, dst_pos, status, N, K, H, nrows, buf, st); break;
+    case 6: err = launch_dispatch<6>(hidden, dst_pos, status, N, K, H, nrows, buf, st); break;
+    case 8: err = launch_dispatch<8>(hidden, dst_pos, status, N, K, H, nrows, buf, st); break;
+    default: err = launch_dispatch<0>(hidden, dst_pos, status, N, K, H, nrows, buf, st); break;
   }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
