@@ -19,7 +19,10 @@ the step list and citations):
   weights (sections 核心技术 and 内存契约与权重布局);
 * :func:`dispatch_backward` / :func:`combine_backward` -- the gradients of the
   fused permute and of the weighted unpermute (section 核心技术 names the
-  pair; their arithmetic is this library's reading, stated in oracle.c).
+  pair; their arithmetic is this library's reading, stated in oracle.c);
+* :func:`grouped_gemm` -- the grouped expert product over the static buffer,
+  group j of rank r times weight row j of the [E+B, H, H'] tensor (section
+  内存契约与权重布局), in double.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (closed forms, brute force, an independent lexsort derivation, hand-worked
@@ -94,6 +97,10 @@ def _load():
                                                  ctypes.c_void_p]
             lib.orc_f32_to_bf16_array.restype = None
             lib.orc_f32_to_bf16_array.argtypes = [ctypes.c_void_p, c_i64, ctypes.c_void_p]
+            lib.orc_grouped_gemm.restype = ctypes.c_int
+            lib.orc_grouped_gemm.argtypes = [ctypes.c_void_p, i32p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_int, c_i64, ctypes.c_int, ctypes.c_int, c_i64,
+                                             c_i64, ctypes.c_void_p, c_i64, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -241,6 +248,35 @@ def combine_backward(dout: np.ndarray, y: np.ndarray, w: np.ndarray, dst_pos: np
     _load().orc_combine_backward(dout.ctypes.data, y.ctypes.data, w.ctypes.data, _i32(dst_pos), N, K,
                                  H, dy.ctypes.data, dw.ctypes.data)
     return dy, dw
+
+
+def grouped_gemm(x: np.ndarray, cu: np.ndarray, w_home: np.ndarray, w_slot: np.ndarray,
+                 rows=None) -> np.ndarray:
+    """y[row] = x[row] @ W_j in double for the buffer rows (all, or ``rows``).
+
+    x is [R*SK, H] bf16 bits, cu [R, E+B] inclusive group ends, w_home
+    [E, H, H'] and w_slot [R, B, H, H'] bf16 bits. Group j of rank r uses
+    w_home[j] (j < E) or w_slot[r, j - E]. Raises ValueError on a bad table."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    cu = np.ascontiguousarray(cu, dtype=np.int32)
+    w_home = np.ascontiguousarray(w_home, dtype=np.uint16)
+    w_slot = np.ascontiguousarray(w_slot, dtype=np.uint16)
+    R, G = cu.shape
+    E, H, Hp = w_home.shape
+    B = G - E
+    assert w_slot.shape == (R, B, H, Hp) and x.shape[1] == H and x.shape[0] % R == 0
+    SK = x.shape[0] // R
+    if rows is None:
+        n, rp = x.shape[0], None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        n, rp = rows.size, rows.ctypes.data
+    y = np.empty((n, Hp), dtype=np.float64)
+    st = _load().orc_grouped_gemm(x.ctypes.data, _i32(cu), w_home.ctypes.data, w_slot.ctypes.data,
+                                  R, SK, E, B, H, Hp, rp, n, y.ctypes.data)
+    if st != 0:
+        raise ValueError(f"grouped_gemm: {STATUS[st]}")
+    return y
 
 
 def f32_to_bf16(x: np.ndarray) -> np.ndarray:

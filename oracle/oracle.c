@@ -453,3 +453,53 @@ void orc_combine_backward(const uint16_t* dout, const uint16_t* y, const float* 
       dw[t * K + k] = acc;
     }
 }
+
+/* Grouped expert product over the static buffer ([umios] 内存契约与权重布局:
+ * one grouped GEMM per projection consumes a single [E+B, H, H'] weight
+ * tensor, rows [0, E) the experts' own weights and rows [E, E+B) the rank's
+ * prefetch slots, and cu_seqlens[E+B] says which of its rows are active).
+ * Rank r's buffer rows [r*SK, (r+1)*SK) hold the groups j = 0..E+B-1 back to
+ * back: group j is rows [cu[r][j-1], cu[r][j]) of that block (cu[r][-1] = 0).
+ * Its weight W_j is w_home[j] for j < E and w_slot[r][j-E] for j >= E, and
+ *   y[row, n] = sum_h x[row, h] * W_j[h, n],
+ * summed in h order in double (every bf16 x bf16 product is exact there) and
+ * returned in double: the caller picks the rounding. rows == NULL means all
+ * R*SK rows in order, else the n_rows listed; y is [n_rows, Hp].
+ * Returns ORC_BAD_ARG, writing nothing, if a cu row is not nondecreasing
+ * from >= 0 to SK or a listed row is out of range. */
+int orc_grouped_gemm(const uint16_t* x, const int32_t* cu, const uint16_t* w_home,
+                     const uint16_t* w_slot, int R, int64_t SK, int E, int B, int64_t H,
+                     int64_t Hp, const int64_t* rows, int64_t n_rows, double* y) {
+  const int G = E + B;
+  int r, j;
+  int64_t q, h, n;
+  for (r = 0; r < R; ++r) {
+    int32_t prev = 0;
+    for (j = 0; j < G; ++j) {
+      if (cu[(int64_t)r * G + j] < prev) return ORC_BAD_ARG;
+      prev = cu[(int64_t)r * G + j];
+    }
+    if (prev != SK) return ORC_BAD_ARG;
+  }
+  for (q = 0; q < n_rows; ++q) {
+    const int64_t row = rows ? rows[q] : q;
+    if (row < 0 || row >= (int64_t)R * SK) return ORC_BAD_ARG;
+  }
+  for (q = 0; q < n_rows; ++q) {
+    const int64_t row = rows ? rows[q] : q;
+    const int64_t i = row % SK;
+    const uint16_t* W;
+    double* out = y + q * Hp;
+    r = (int)(row / SK);
+    j = 0; /* the group holding local row i: the first j whose end exceeds i */
+    while (cu[(int64_t)r * G + j] <= i) ++j;
+    W = j < E ? w_home + (int64_t)j * H * Hp : w_slot + ((int64_t)r * B + (j - E)) * H * Hp;
+    for (n = 0; n < Hp; ++n) out[n] = 0.0;
+    for (h = 0; h < H; ++h) {
+      const double xv = (double)orc_bf16_to_f32(x[row * H + h]);
+      const uint16_t* wrow = W + h * Hp;
+      for (n = 0; n < Hp; ++n) out[n] += xv * (double)orc_bf16_to_f32(wrow[n]);
+    }
+  }
+  return ORC_OK;
+}
