@@ -46,7 +46,20 @@ constexpr int kUnroll = MEP_DISPATCH_UNROLL;
 #ifndef MEP_COMBINE_UNROLL
 #define MEP_COMBINE_UNROLL 2
 #endif
-constexpr int kCombineUnroll = MEP_COMBINE_UNROLL;  // column vectors per lane in flight
+#ifndef MEP_COMBINE_UNROLL32
+#define MEP_COMBINE_UNROLL32 2
+#endif
+#ifndef MEP_COMBINE_V32
+#define MEP_COMBINE_V32 1
+#endif
+#ifndef MEP_CBWD_V32
+#define MEP_CBWD_V32 1
+#endif
+#ifndef MEP_CBWD_V32_MIN_H
+#define MEP_CBWD_V32_MIN_H 4096
+#endif
+constexpr int kCombineUnroll = MEP_COMBINE_UNROLL;      // 16-byte column vectors per lane in flight
+constexpr int kCombineUnroll32 = MEP_COMBINE_UNROLL32;  // 32-byte column vectors per lane in flight
 
 // 16- and 32-byte vectors. The 32-byte forms (ld/st .v8.b32, sm_100 and
 // later) halve the memory instructions per byte; they need 32-byte aligned
@@ -73,6 +86,36 @@ __device__ __forceinline__ void st_cs(Vec32* p, const Vec32& v) {
                "r"(v.w[6]), "r"(v.w[7])
                : "memory");
 }
+
+__device__ __forceinline__ void st_plain(uint4* p, const uint4& v) { *p = v; }
+__device__ __forceinline__ void st_plain(Vec32* p, const Vec32& v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+               "r"(v.w[7])
+               : "memory");
+}
+
+// 32-bit words of a vector (2 bf16 each): 4 for uint4, 8 for Vec32.
+template <typename V> struct Words;
+template <> struct Words<uint4> {
+  static constexpr int n = 4;
+  static __device__ __forceinline__ uint32_t get(const uint4& q, int j) {
+    return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+  }
+  static __device__ __forceinline__ uint4 make(const uint32_t (&o)[4]) {
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+};
+template <> struct Words<Vec32> {
+  static constexpr int n = 8;
+  static __device__ __forceinline__ uint32_t get(const Vec32& q, int j) { return q.w[j]; }
+  static __device__ __forceinline__ Vec32 make(const uint32_t (&o)[8]) {
+    Vec32 v;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v.w[j] = o[j];
+    return v;
+  }
+};
 
 inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
@@ -157,36 +200,39 @@ cudaError_t launch_dispatch(const void* x, const int32_t* dst, int32_t* status, 
 }
 
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void fma8(float (&acc)[8], float w, uint4 q) {
-  const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+// acc[i] = fma(w, bf16 element i of q, acc[i]) for the 2n elements of q
+template <typename V>
+__device__ __forceinline__ void fmaV(float (&acc)[2 * Words<V>::n], float w, const V& q) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float lo = __uint_as_float(v[j] << 16);
-    const float hi = __uint_as_float(v[j] & 0xffff0000u);
-    acc[2 * j] = __fmaf_rn(w, lo, acc[2 * j]);
-    acc[2 * j + 1] = __fmaf_rn(w, hi, acc[2 * j + 1]);
+  for (int j = 0; j < Words<V>::n; ++j) {
+    const uint32_t v = Words<V>::get(q, j);
+    acc[2 * j] = __fmaf_rn(w, __uint_as_float(v << 16), acc[2 * j]);
+    acc[2 * j + 1] = __fmaf_rn(w, __uint_as_float(v & 0xffff0000u), acc[2 * j + 1]);
   }
 }
 
-__device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
-  uint32_t o[4];
+template <typename V>
+__device__ __forceinline__ V packV(const float (&acc)[2 * Words<V>::n]) {
+  uint32_t o[Words<V>::n];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < Words<V>::n; ++j) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
     o[j] = *reinterpret_cast<const uint32_t*>(&h);
   }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+  return Words<V>::make(o);
 }
 
 // KT > 0: K known at compile time (all K gathers of a vector in flight at
 // once). KT == 0: any K, gathered in batches of 8. UNIT: every weight is 1
 // and topk_w is not read (the backward of dispatch: sum of the K rows; an fma
 // with 1 rounds exactly like an add).
-template <int KT, bool UNIT = false>
+template <int KT, bool UNIT, typename V>
 __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
-    k_combine(const uint4* __restrict__ y, const float* __restrict__ topk_w,
+    k_combine(const V* __restrict__ y, const float* __restrict__ topk_w,
               const int32_t* __restrict__ dst_pos, int32_t* status, long long N, int Kr,
-              long long vpr, long long nrows, uint4* __restrict__ out) {
+              long long vpr, long long nrows, V* __restrict__ out) {
+  constexpr int U = sizeof(V) == 32 ? kCombineUnroll32 : kCombineUnroll;
+  constexpr int NE = 2 * Words<V>::n;  // bf16 elements per vector
   pdl_wait();
   pdl_launch_dependents();
   if (read_status(status) != 0) return;
@@ -204,7 +250,7 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
       if (lane == 0) set_status(status, MEP_ERR_BAD_POSITION);
       continue;
     }
-    uint4* o = out + t * vpr;
+    V* o = out + t * vpr;
     if constexpr (KT > 0) {
       long long rows[KT];
       float ws[KT];
@@ -213,28 +259,32 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
         rows[k] = (long long)__shfl_sync(MEP_FULL_MASK, r0, k) * vpr;
         ws[k] = __shfl_sync(MEP_FULL_MASK, w0, k);
       }
-      for (long long v0 = lane; v0 < vpr; v0 += 32 * kCombineUnroll) {
-        uint4 q[kCombineUnroll][KT];
+      for (long long v0 = lane; v0 < vpr; v0 += 32 * U) {
+        V q[U][KT];
 #pragma unroll
-        for (int u = 0; u < kCombineUnroll; ++u)
+        for (int u = 0; u < U; ++u)
           if (v0 + 32 * u < vpr) {
 #pragma unroll
-            for (int k = 0; k < KT; ++k) q[u][k] = __ldg(y + rows[k] + v0 + 32 * u);
+            for (int k = 0; k < KT; ++k) q[u][k] = ld_nc(y + rows[k] + v0 + 32 * u);
           }
 #pragma unroll
-        for (int u = 0; u < kCombineUnroll; ++u)
+        for (int u = 0; u < U; ++u)
           if (v0 + 32 * u < vpr) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float acc[NE];
 #pragma unroll
-            for (int k = 0; k < KT; ++k) fma8(acc, ws[k], q[u][k]);
-            o[v0 + 32 * u] = pack8(acc);
+            for (int i = 0; i < NE; ++i) acc[i] = 0.f;
+#pragma unroll
+            for (int k = 0; k < KT; ++k) fmaV<V>(acc, ws[k], q[u][k]);
+            st_plain(o + v0 + 32 * u, packV<V>(acc));
           }
       }
     } else {
       for (long long v = lane; v < vpr; v += 32) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float acc[NE];
+#pragma unroll
+        for (int i = 0; i < NE; ++i) acc[i] = 0.f;
         for (int k0 = 0; k0 < K; k0 += 8) {
-          uint4 q[8];
+          V q[8];
           float ws[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -242,57 +292,63 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
             if (k < K) {
               const long long row = __ldg(dst_pos + t * K + k);
               ws[j] = UNIT ? 1.f : __ldg(topk_w + t * K + k);
-              q[j] = __ldg(y + row * vpr + v);
+              q[j] = ld_nc(y + row * vpr + v);
             }
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            if (k0 + j < K) fma8(acc, ws[j], q[j]);
+            if (k0 + j < K) fmaV<V>(acc, ws[j], q[j]);
         }
-        o[v] = pack8(acc);
+        st_plain(o + v, packV<V>(acc));
       }
     }
   }
 }
 
 template <int KT, bool UNIT = false>
-cudaError_t launch_combine(const uint4* y, const float* w, const int32_t* dst, int32_t* status,
-                           long long N, int K, long long vpr, long long nrows, uint4* out,
+cudaError_t launch_combine(const void* y, const float* w, const int32_t* dst, int32_t* status,
+                           long long N, int K, int H, long long nrows, void* out,
                            cudaStream_t st) {
   const long long want = (N + MEP_COMBINE_WARPS - 1) / MEP_COMBINE_WARPS;
   const long long cap = (long long)sm_count() * 64;
   const int grid = int(want < cap ? want : cap);
-  return launch_pdl(k_combine<KT, UNIT>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0, st, y, w,
-                    dst, status, N, K, vpr, nrows, out);
+  if (MEP_COMBINE_V32 && H % 16 == 0 && aligned32(y) && aligned32(out))
+    return launch_pdl(k_combine<KT, UNIT, Vec32>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0,
+                      st, static_cast<const Vec32*>(y), w, dst, status, N, K, (long long)(H / 16),
+                      nrows, static_cast<Vec32*>(out));
+  return launch_pdl(k_combine<KT, UNIT, uint4>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0, st,
+                    static_cast<const uint4*>(y), w, dst, status, N, K, (long long)(H / 8), nrows,
+                    static_cast<uint4*>(out));
 }
 
 // ---------------------------------------------------------------------------
-// Backward of combine, one warp per token. Per 16-byte column vector v: load
+// Backward of combine, one warp per token. Per column vector v: load
 // dout[t, v] and the K rows y[dst_pos[t,k], v]; write
 //   dy[dst_pos[t,k], v] = bf16_rn(fp32(w[t,k] * dout[t, v]))   (streaming)
 // and accumulate the K dot products <dout[t], y[dst_pos[t,k]]> per lane with
 // fp32 fma (every bf16 x bf16 product is exact in fp32), then reduce them
 // across the warp (butterfly) and write dw[t, k] from lane 0.
-__device__ __forceinline__ uint4 scale8(float w, uint4 q) {
-  const uint32_t v[4] = {q.x, q.y, q.z, q.w};
-  uint32_t o[4];
+template <typename V>
+__device__ __forceinline__ V scaleV(float w, const V& q) {
+  uint32_t o[Words<V>::n];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float lo = __fmul_rn(w, __uint_as_float(v[j] << 16));
-    const float hi = __fmul_rn(w, __uint_as_float(v[j] & 0xffff0000u));
+  for (int j = 0; j < Words<V>::n; ++j) {
+    const uint32_t v = Words<V>::get(q, j);
+    const float lo = __fmul_rn(w, __uint_as_float(v << 16));
+    const float hi = __fmul_rn(w, __uint_as_float(v & 0xffff0000u));
     const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     o[j] = *reinterpret_cast<const uint32_t*>(&h);
   }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+  return Words<V>::make(o);
 }
 
-__device__ __forceinline__ float dot8(float acc, uint4 a, uint4 b) {
-  const uint32_t va[4] = {a.x, a.y, a.z, a.w};
-  const uint32_t vb[4] = {b.x, b.y, b.z, b.w};
+template <typename V>
+__device__ __forceinline__ float dotV(float acc, const V& a, const V& b) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    acc = __fmaf_rn(__uint_as_float(va[j] << 16), __uint_as_float(vb[j] << 16), acc);
-    acc = __fmaf_rn(__uint_as_float(va[j] & 0xffff0000u), __uint_as_float(vb[j] & 0xffff0000u), acc);
+  for (int j = 0; j < Words<V>::n; ++j) {
+    const uint32_t va = Words<V>::get(a, j), vb = Words<V>::get(b, j);
+    acc = __fmaf_rn(__uint_as_float(va << 16), __uint_as_float(vb << 16), acc);
+    acc = __fmaf_rn(__uint_as_float(va & 0xffff0000u), __uint_as_float(vb & 0xffff0000u), acc);
   }
   return acc;
 }
@@ -303,12 +359,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <int KT>
+template <int KT, typename V>
 __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
-    k_combine_backward(const uint4* __restrict__ dout, const uint4* __restrict__ y,
+    k_combine_backward(const V* __restrict__ dout, const V* __restrict__ y,
                        const float* __restrict__ topk_w, const int32_t* __restrict__ dst_pos,
                        int32_t* status, long long N, int Kr, long long vpr, long long nrows,
-                       uint4* __restrict__ dy, float* __restrict__ dw) {
+                       V* __restrict__ dy, float* __restrict__ dw) {
   pdl_wait();
   pdl_launch_dependents();
   if (read_status(status) != 0) return;
@@ -326,7 +382,7 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
       if (lane == 0) set_status(status, MEP_ERR_BAD_POSITION);
       continue;
     }
-    const uint4* d = dout + t * vpr;
+    const V* d = dout + t * vpr;
     if constexpr (KT > 0) {
       long long rows[KT];
       float ws[KT], acc[KT];
@@ -337,14 +393,14 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
         acc[k] = 0.f;
       }
       for (long long v = lane; v < vpr; v += 32) {
-        const uint4 g = __ldg(d + v);
-        uint4 q[KT];
+        const V g = ld_nc(d + v);
+        V q[KT];
 #pragma unroll
-        for (int k = 0; k < KT; ++k) q[k] = __ldg(y + rows[k] + v);
+        for (int k = 0; k < KT; ++k) q[k] = ld_nc(y + rows[k] + v);
 #pragma unroll
         for (int k = 0; k < KT; ++k) {
-          __stcs(dy + rows[k] + v, scale8(ws[k], g));
-          acc[k] = dot8(acc[k], g, q[k]);
+          st_cs(dy + rows[k] + v, scaleV<V>(ws[k], g));
+          acc[k] = dotV<V>(acc[k], g, q[k]);
         }
       }
 #pragma unroll
@@ -358,9 +414,9 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
         const float wk = __ldg(topk_w + t * K + k);
         float acc = 0.f;
         for (long long v = lane; v < vpr; v += 32) {
-          const uint4 g = __ldg(d + v);
-          __stcs(dy + row + v, scale8(wk, g));
-          acc = dot8(acc, g, __ldg(y + row + v));
+          const V g = ld_nc(d + v);
+          st_cs(dy + row + v, scaleV<V>(wk, g));
+          acc = dotV<V>(acc, g, ld_nc(y + row + v));
         }
         const float s = warp_sum(acc);
         if (lane == 0) dw[t * K + k] = s;
@@ -370,15 +426,24 @@ __global__ void __launch_bounds__(32 * MEP_COMBINE_WARPS)
 }
 
 template <int KT>
-cudaError_t launch_combine_backward(const uint4* dout, const uint4* y, const float* w,
+cudaError_t launch_combine_backward(const void* dout, const void* y, const float* w,
                                     const int32_t* dst, int32_t* status, long long N, int K,
-                                    long long vpr, long long nrows, uint4* dy, float* dw,
+                                    int H, long long nrows, void* dy, float* dw,
                                     cudaStream_t st) {
   const long long want = (N + MEP_COMBINE_WARPS - 1) / MEP_COMBINE_WARPS;
   const long long cap = (long long)sm_count() * 64;
   const int grid = int(want < cap ? want : cap);
-  return launch_pdl(k_combine_backward<KT>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0, st,
-                    dout, y, w, dst, status, N, K, vpr, nrows, dy, dw);
+  // 32-byte vectors pay off once a lane walks 8 or more of them per row;
+  // below that the 16-byte form keeps more rows in flight (measured: 3% faster
+  // at H = 2048, 4% slower at H = 7168).
+  if (MEP_CBWD_V32 && H % 16 == 0 && H >= MEP_CBWD_V32_MIN_H && aligned32(dout) && aligned32(y) &&
+      aligned32(dy))
+    return launch_pdl(k_combine_backward<KT, Vec32>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0,
+                      st, static_cast<const Vec32*>(dout), static_cast<const Vec32*>(y), w, dst,
+                      status, N, K, (long long)(H / 16), nrows, static_cast<Vec32*>(dy), dw);
+  return launch_pdl(k_combine_backward<KT, uint4>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0,
+                    st, static_cast<const uint4*>(dout), static_cast<const uint4*>(y), w, dst,
+                    status, N, K, (long long)(H / 8), nrows, static_cast<uint4*>(dy), dw);
 }
 
 }  // namespace
@@ -424,19 +489,16 @@ extern "C" int mep_combine(const mep_bf16* y, const float* topk_w, const int32_t
   const long long N = (long long)R * S;
   if (N == 0) return MEP_OK;
   if (topk_w == nullptr) return MEP_ERR_INVALID_ARG;
-  const long long vpr = H / 8;
-  const uint4* y4 = reinterpret_cast<const uint4*>(y);
-  uint4* o4 = reinterpret_cast<uint4*>(out);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long long nrows = N * K;
   cudaError_t err;
   switch (K) {
-    case 1: err = launch_combine<1>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    case 2: err = launch_combine<2>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    case 4: err = launch_combine<4>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    case 6: err = launch_combine<6>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    case 8: err = launch_combine<8>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    default: err = launch_combine<0>(y4, topk_w, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+    case 1: err = launch_combine<1>(y, topk_w, dst_pos, status, N, K, H, nrows, out, st); break;
+    case 2: err = launch_combine<2>(y, topk_w, dst_pos, status, N, K, H, nrows, out, st); break;
+    case 4: err = launch_combine<4>(y, topk_w, dst_pos, status, N, K, H, nrows, out, st); break;
+    case 6: err = launch_combine<6>(y, topk_w, dst_pos, status, N, K, H, nrows, out, st); break;
+    case 8: err = launch_combine<8>(y, topk_w, dst_pos, status, N, K, H, nrows, out, st); break;
+    default: err = launch_combine<0>(y, topk_w, dst_pos, status, N, K, H, nrows, out, st); break;
   }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
@@ -448,19 +510,16 @@ extern "C" int mep_dispatch_backward(const mep_bf16* dbuf, const int32_t* dst_po
   if (rc != MEP_OK) return rc;
   const long long N = (long long)R * S;
   if (N == 0) return MEP_OK;
-  const long long vpr = H / 8;
-  const uint4* g4 = reinterpret_cast<const uint4*>(dbuf);
-  uint4* o4 = reinterpret_cast<uint4*>(dhidden);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long long nrows = N * K;
   cudaError_t err;
   switch (K) {
-    case 1: err = launch_combine<1, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    case 2: err = launch_combine<2, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    case 4: err = launch_combine<4, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    case 6: err = launch_combine<6, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    case 8: err = launch_combine<8, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
-    default: err = launch_combine<0, true>(g4, nullptr, dst_pos, status, N, K, vpr, nrows, o4, st); break;
+    case 1: err = launch_combine<1, true>(dbuf, nullptr, dst_pos, status, N, K, H, nrows, dhidden, st); break;
+    case 2: err = launch_combine<2, true>(dbuf, nullptr, dst_pos, status, N, K, H, nrows, dhidden, st); break;
+    case 4: err = launch_combine<4, true>(dbuf, nullptr, dst_pos, status, N, K, H, nrows, dhidden, st); break;
+    case 6: err = launch_combine<6, true>(dbuf, nullptr, dst_pos, status, N, K, H, nrows, dhidden, st); break;
+    case 8: err = launch_combine<8, true>(dbuf, nullptr, dst_pos, status, N, K, H, nrows, dhidden, st); break;
+    default: err = launch_combine<0, true>(dbuf, nullptr, dst_pos, status, N, K, H, nrows, dhidden, st); break;
   }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
@@ -474,20 +533,16 @@ extern "C" int mep_combine_backward(const mep_bf16* dout, const mep_bf16* y, con
   if (N == 0) return MEP_OK;
   if (topk_w == nullptr || dy == nullptr || dw == nullptr || !aligned16(dy))
     return MEP_ERR_INVALID_ARG;
-  const long long vpr = H / 8;
-  const uint4* d4 = reinterpret_cast<const uint4*>(dout);
-  const uint4* y4 = reinterpret_cast<const uint4*>(y);
-  uint4* dy4 = reinterpret_cast<uint4*>(dy);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long long nrows = N * K;
   cudaError_t err;
   switch (K) {
-    case 1: err = launch_combine_backward<1>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
-    case 2: err = launch_combine_backward<2>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
-    case 4: err = launch_combine_backward<4>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
-    case 6: err = launch_combine_backward<6>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
-    case 8: err = launch_combine_backward<8>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
-    default: err = launch_combine_backward<0>(d4, y4, topk_w, dst_pos, status, N, K, vpr, nrows, dy4, dw, st); break;
+    case 1: err = launch_combine_backward<1>(dout, y, topk_w, dst_pos, status, N, K, H, nrows, dy, dw, st); break;
+    case 2: err = launch_combine_backward<2>(dout, y, topk_w, dst_pos, status, N, K, H, nrows, dy, dw, st); break;
+    case 4: err = launch_combine_backward<4>(dout, y, topk_w, dst_pos, status, N, K, H, nrows, dy, dw, st); break;
+    case 6: err = launch_combine_backward<6>(dout, y, topk_w, dst_pos, status, N, K, H, nrows, dy, dw, st); break;
+    case 8: err = launch_combine_backward<8>(dout, y, topk_w, dst_pos, status, N, K, H, nrows, dy, dw, st); break;
+    default: err = launch_combine_backward<0>(dout, y, topk_w, dst_pos, status, N, K, H, nrows, dy, dw, st); break;
   }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
