@@ -9,6 +9,7 @@
  *   mep_reduce_grad redundant-slot gradients folded into home gradients
  *   mep_prefetch    redundant experts' weights copied into their slots
  *   mep_dispatch_backward / mep_combine_backward   the two permutes' gradients
+ *   mep_grouped_gemm  the grouped expert product that consumes the buffer
  *
  * Sources (web pages about MoonEP, cited by title and section):
  *   "月之暗面开源MoonEP：面向MoE训练的专家并行通信库" -- sections
@@ -64,7 +65,8 @@ typedef uint16_t mep_bf16;
 #define MEP_ERR_CAPACITY 4      /* device: some rank needs more than B redundant slots */
 #define MEP_ERR_BAD_POSITION 5  /* device: a dst_pos entry outside [0, R*S*K) */
 #define MEP_ERR_BAD_SLOT_MAP 6  /* device: a slot_expert entry outside [-1, E) */
-#define MEP_ERR_TIMEOUT 7       /* device: a bounded wait gave up (reserved: no kernel waits today) */
+#define MEP_ERR_TIMEOUT 7       /* device: a bounded pipeline wait inside mep_grouped_gemm gave up */
+#define MEP_ERR_BAD_SEQLENS 8   /* device: a cu_seqlens row decreases, is negative or does not end at S*K */
 
 /* Size limits checked on the host. */
 #define MEP_MAX_E 4096     /* experts */
@@ -254,7 +256,9 @@ MEP_API int mep_dispatch_backward(const mep_bf16* dbuf, const int32_t* dst_pos, 
  *   dw[t, k]            = sum_h dout[t,h] * y[dst_pos[t,k], h]   (fp32)
  * Every bf16 x bf16 product is exact in fp32; the dw sum is accumulated in
  * fp32 (per lane, then across a warp), so it matches the exact dot product to
- * within (H/32 + 6) * 2^-24 * sum_h |dout[t,h] * y[dst_pos[t,k],h]|.
+ * within (n + 5) * 2^-24 * sum_h |dout[t,h] * y[dst_pos[t,k],h]|, where
+ * n = ceil(H / (32 c)) * c is the longest per-lane chain, c = 16 when
+ * H % 16 == 0 and 8 otherwise (the bf16 elements per column vector).
  *   dout     bf16 [R*S, H]     gradient of combine's output
  *   y        bf16 [R*S*K, H]   combine's input (expert outputs)
  *   topk_w   fp32 [R*S, K]     routing weights
@@ -288,6 +292,41 @@ MEP_API int mep_combine_backward(const mep_bf16* dout, const mep_bf16* y, const 
  */
 MEP_API int mep_reduce_grad(const int32_t* slot_expert, int E, int R, int B, int64_t HHp,
                     float* home_grad, float* slot_grad, int32_t* status, void* stream);
+
+/*
+ * mep_grouped_gemm -- the grouped expert product over the static buffer
+ * ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库", 内存契约与权重布局: one
+ * grouped GEMM per expert projection consumes a single [E+B, H, H'] weight
+ * tensor -- rows [0, E) the experts' own weights, rows [E, E+B) the rank's
+ * prefetch slots -- and cu_seqlens[E+B] says which buffer rows each weight
+ * row serves). For rank r, group j spans rows [cu[r][j-1], cu[r][j]) of the
+ * rank's block [r*S*K, (r+1)*S*K) of x (cu[r][-1] = 0), and
+ *   y[row, n] = bf16_rn( sum_h x[row, h] * W_j[h, n] ),
+ *   W_j = w_home[j] for j < E,  w_slot[r][j - E] for j >= E,
+ * with the sum accumulated in fp32 by the tensor cores (tcgen05, order
+ * unspecified). Rows of an inference plan's overflow (mep_plan_remote_fallback)
+ * sit in home rows j < E of a non-home rank and so read w_home[j] directly.
+ *   x          bf16 [R*S*K, H]       the dispatch buffer (or any rows so grouped)
+ *   cu_seqlens int32 [R, E+B]        inclusive group ends, from mep_plan
+ *   w_home     bf16 [E, H, H']       experts' weights
+ *   w_slot     bf16 [R, B, H, H']    prefetch slots (mep_prefetch); may be NULL when B == 0
+ *   status     int32 [1]             read on entry (nonzero: no-op); set to
+ *                                    MEP_ERR_BAD_SEQLENS (y untouched) for a
+ *                                    malformed cu_seqlens row, or MEP_ERR_TIMEOUT
+ *                                    if a pipeline wait gives up. May be NULL.
+ *   H          multiple of 64;  Hp (= H') multiple of 8
+ *   ws         device workspace of at least mep_grouped_gemm_workspace_bytes
+ *              (the tile table, rebuilt by every call)
+ *   y          bf16 [R*S*K, H']      output, every row written; must not overlap
+ *              the inputs
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG (sizes, null pointers, alignment:
+ * every tensor 16-byte aligned), MEP_ERR_CUDA.
+ */
+MEP_API int mep_grouped_gemm_workspace_bytes(int R, int S, int K, int E, int B, size_t* bytes);
+MEP_API int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens, const mep_bf16* w_home,
+                             const mep_bf16* w_slot, int32_t* status, int R, int S, int K, int E,
+                             int B, int H, int Hp, void* ws, size_t ws_bytes, mep_bf16* y,
+                             void* stream);
 
 #ifdef __cplusplus
 }

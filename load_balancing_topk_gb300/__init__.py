@@ -49,6 +49,7 @@ STATUS = {
     5: "MEP_ERR_BAD_POSITION",
     6: "MEP_ERR_BAD_SLOT_MAP",
     7: "MEP_ERR_TIMEOUT",
+    8: "MEP_ERR_BAD_SEQLENS",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
@@ -68,6 +69,9 @@ SIGNATURES = [
     ("mep_prefetch", _I, [_VP, _I, _I, _I, ctypes.c_int64, _VP, _VP, _VP, _VP]),
     ("mep_dispatch_backward", _I, [_VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP]),
     ("mep_combine_backward", _I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP]),
+    ("mep_grouped_gemm_workspace_bytes", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
+    ("mep_grouped_gemm", _I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, ctypes.c_size_t,
+                              _VP, _VP]),
 ]
 
 
@@ -120,6 +124,13 @@ def plan_workspace_bytes(R: int, S: int, K: int, E: int, B: int) -> int:
     out = ctypes.c_size_t(0)
     _check("mep_plan_workspace_bytes",
            load_library().mep_plan_workspace_bytes(R, S, K, E, B, ctypes.byref(out)))
+    return int(out.value)
+
+
+def grouped_gemm_workspace_bytes(R: int, S: int, K: int, E: int, B: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check("mep_grouped_gemm_workspace_bytes",
+           load_library().mep_grouped_gemm_workspace_bytes(R, S, K, E, B, ctypes.byref(out)))
     return int(out.value)
 
 
@@ -371,3 +382,45 @@ def mep_combine_backward(dout, y, topk_w, dst_pos, status, R: int, S: int, K: in
                                                  _stream(dev))
     _check("mep_combine_backward", rc)
     return dy, dw
+
+
+def mep_grouped_gemm(x, cu_seqlens, w_home, w_slot, status, R: int, S: int, K: int,
+                     y=None, workspace=None):
+    """y[row] = bf16(x[row] @ W_j) for the group j of every buffer row.
+
+    x: bf16 [R*S*K, H] (the dispatch buffer); cu_seqlens: int32 [R, E+B];
+    w_home: bf16 [E, H, H']; w_slot: bf16 [R, B, H, H'] (None when B == 0).
+    Group j of rank r uses w_home[j] below E and w_slot[r, j - E] above.
+    Returns y, bf16 [R*S*K, H'].
+    """
+    torch = _torch()
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    _need(w_home, "w_home", torch.bfloat16, None, dev)
+    E, H, Hp = w_home.shape
+    _need(cu_seqlens, "cu_seqlens", torch.int32, None, dev)
+    if cu_seqlens.dim() != 2 or cu_seqlens.shape[0] != R:
+        raise ValueError("cu_seqlens must be [R, E+B]")
+    B = cu_seqlens.shape[1] - E
+    if B < 0:
+        raise ValueError("cu_seqlens must have E+B columns")
+    if x.numel() != R * S * K * H:
+        raise ValueError("x must hold R*S*K rows of H")
+    if B > 0:
+        _need(w_slot, "w_slot", torch.bfloat16, (R, B, H, Hp), dev)
+    if status is not None:
+        _need(status, "status", torch.int32, (1,), dev)
+    if y is None:
+        y = torch.empty((R * S * K, Hp), dtype=torch.bfloat16, device=dev)
+    else:
+        _need(y, "y", torch.bfloat16, (R * S * K, Hp), dev)
+    need = grouped_gemm_workspace_bytes(R, S, K, E, B)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = load_library().mep_grouped_gemm(_ptr(x), _ptr(cu_seqlens), _ptr(w_home),
+                                             _ptr(w_slot) if B > 0 else None, _ptr(status), R, S,
+                                             K, E, B, H, Hp, _ptr(workspace), need, _ptr(y),
+                                             _stream(dev))
+    _check("mep_grouped_gemm", rc)
+    return y

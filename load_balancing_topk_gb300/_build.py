@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libmep.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["abi.cu", "plan.cu", "permute.cu", "reduce_grad.cu", "prefetch.cu", "plan_static.cu"]
+SOURCES = ["abi.cu", "plan.cu", "permute.cu", "reduce_grad.cu", "prefetch.cu", "plan_static.cu",
+           "grouped_gemm.cu"]
 
 
 def nvcc() -> str:

@@ -46,6 +46,7 @@ extern "C" const char* mep_status_string(int code) {
     case MEP_ERR_BAD_POSITION: return "bad position: dst_pos entry out of range";
     case MEP_ERR_BAD_SLOT_MAP: return "bad slot map: slot_expert entry out of range";
     case MEP_ERR_TIMEOUT: return "timeout: a bounded wait inside a kernel gave up";
+    case MEP_ERR_BAD_SEQLENS: return "bad cu_seqlens: a row decreases, is negative or does not end at S*K";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,520 @@
+// grouped_gemm.cu -- the grouped expert product over the static buffer
+// (mep_grouped_gemm), on the sm_100-family tensor cores (tcgen05 + TMA).
+//
+// Source: "月之暗面开源MoonEP：面向MoE训练的专家并行通信库", section
+// 内存契约与权重布局: one grouped GEMM per expert projection consumes a single
+// [E+B, H, H'] weight tensor (rows [0, E) the experts' own weights, rows
+// [E, E+B) the rank's prefetch slots) and cu_seqlens[E+B] says which rows of
+// the static S*K buffer each weight row serves.
+//
+// Two launches on the caller's stream:
+//   k_gemm_tiles  (1 CTA) checks every cu_seqlens row and cuts every group
+//                 into 128-row tiles {first buffer row, rows, weight row},
+//                 written to the workspace with their count;
+//   k_gemm        (persistent, one CTA per SM, 192 threads) walks the work
+//                 units (tile, 256-column block of H') grid-stride:
+//     warp 0      TMA producer: per 64-wide K step, a 128x64 tile of x
+//                 (K-major, 128-byte swizzle) and up to four 64x64 boxes of
+//                 the weight row (H' contiguous: MN-major, 128-byte swizzle)
+//                 into a 4-stage shared-memory ring;
+//     warp 1      owns the TMEM allocation (2 x 256 fp32 columns) and, from
+//                 one lane, issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
+//                 fp32 accumulate) and the commits that free ring stages and
+//                 hand finished accumulators to the epilogue;
+//     warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
+//                 round to bf16 (nearest-even) and store the valid rows and
+//                 columns; the accumulator is double-buffered, so the next
+//                 unit's MMAs overlap this store.
+// Every wait is bounded (MEP_GEMM_TIMEOUT_NS on %globaltimer): a wait that
+// gives up raises a CTA-wide abort flag and MEP_ERR_TIMEOUT; every role then
+// leaves its loop, the producer waits for its own copies in flight, the MMA
+// lane for its own MMAs, and the TMEM is freed before the CTA exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "mep_common.cuh"
+
+#ifndef MEP_GEMM_B_LBO
+#define MEP_GEMM_B_LBO 8192  // byte stride between 64-wide H' blocks of a weight stage
+#endif
+#ifndef MEP_GEMM_B_SBO
+#define MEP_GEMM_B_SBO 1024  // byte stride between 8-row K groups of a weight stage
+#endif
+#ifndef MEP_GEMM_TIMEOUT_NS
+#define MEP_GEMM_TIMEOUT_NS 4000000000ull
+#endif
+
+namespace mep {
+namespace {
+
+constexpr int kBM = 128;                   // tile rows (TMEM lanes)
+constexpr int kBN = 256;                   // tile columns of H' (TMEM columns per accumulator)
+constexpr int kBK = 64;                    // K step: one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;     // 16 KB
+constexpr int kBBox = kBK * 64 * 2;        // one 64x64 weight box, 8 KB
+constexpr int kBBytes = 4 * kBBox;         // 32 KB
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 2 * kBN;         // double-buffered accumulator
+constexpr int kTileThreads = 1024;
+constexpr int kSmemBytes = 1024 /* alignment slack */ + kStages * (kABytes + kBBytes) + 256;
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (mbarrier, TMA, tcgen05)
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete.
+// Returns false on timeout (raising the abort flag and MEP_ERR_TIMEOUT) and,
+// when honor_abort, as soon as another role has raised the flag. The drains
+// at the end of the kernel pass honor_abort = false: they must see their own
+// copies and MMAs land before the CTA frees its TMEM and exits.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             int32_t* status, bool honor_abort) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (honor_abort && *abort) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > MEP_GEMM_TIMEOUT_NS) {
+        *abort = 1;
+        set_status(status, MEP_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort,
+                                           int32_t* status, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, abort, status, honor_abort);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1 (bits 46-47) and the
+// 128-byte swizzle layout (value 2 in bits 61-63). Stage buffers are
+// 1024-byte aligned, so the base-offset field stays 0.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and
+// B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B MN-major
+// (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                            ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes, one lane (row)
+// per thread.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// Tile table. tiles[i] = {first buffer row, rows (1..128), weight row, 0}
+// where weight row < E is a home expert and E + r*B + b is slot b of rank r.
+__global__ void __launch_bounds__(kTileThreads)
+    k_gemm_tiles(const int32_t* __restrict__ cu, int R, int E, int B, int SK, int32_t* status,
+                 int4* __restrict__ tiles, int* __restrict__ count) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ int s_warp[33];
+  __shared__ int s_bad, s_carry, s_stat;
+  const int G = E + B;
+  const long long RG = (long long)R * G;
+  if (threadIdx.x == 0) {
+    s_bad = 0;
+    s_carry = 0;
+    s_stat = read_status(status);
+  }
+  __syncthreads();
+  if (s_stat != 0) {
+    if (threadIdx.x == 0) *count = 0;
+    return;
+  }
+  // every row nondecreasing from >= 0 and ending at S*K
+  for (long long p = threadIdx.x; p < RG; p += blockDim.x) {
+    const int j = int(p % G);
+    const int v = cu[p];
+    const int prev = j == 0 ? 0 : cu[p - 1];
+    if (v < prev || (j == G - 1 && v != SK)) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) {
+      *count = 0;
+      set_status(status, MEP_ERR_BAD_SEQLENS);
+    }
+    return;
+  }
+  __shared__ int s_nt[kTileThreads + 1];
+  for (long long base = 0; base < RG; base += blockDim.x) {
+    const long long p = base + threadIdx.x;
+    int lo = 0, len = 0;
+    if (p < RG) {
+      const int j = int(p % G);
+      lo = j == 0 ? 0 : cu[p - 1];
+      len = cu[p] - lo;
+    }
+    s_nt[threadIdx.x] = (len + kBM - 1) / kBM;
+    __syncthreads();
+    block_excl_scan(s_nt, s_nt, blockDim.x, s_warp, true);
+    if (p < RG && len > 0) {
+      const int r = int(p / G), j = int(p % G);
+      const int widx = j < E ? j : E + r * B + (j - E);
+      const long long row0 = (long long)r * SK + lo;
+      int off = s_carry + s_nt[threadIdx.x];
+      for (int m = 0; m * kBM < len; ++m, ++off)
+        tiles[off] = make_int4(int(row0 + (long long)m * kBM), min(kBM, len - m * kBM), widx, 0);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s_carry += s_nt[blockDim.x];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *count = s_carry;
+}
+
+// ---------------------------------------------------------------------------
+struct GemmSmem {
+  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain;
+  uint32_t tmem;
+  int abort;
+  int count;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wh,
+           const __grid_constant__ CUtensorMap map_ws, const int4* __restrict__ tiles,
+           const int* __restrict__ count_ptr, int32_t* status, int E, int H, int Hp,
+           __nv_bfloat16* __restrict__ y) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzled stages want 1024-byte alignment
+  uint8_t* gen_base = smem_raw + (base - raw);
+  const uint32_t sa = base;                      // A stages
+  const uint32_t sb = base + kStages * kABytes;  // B stages
+  GemmSmem* S = reinterpret_cast<GemmSmem*>(gen_base + kStages * (kABytes + kBBytes));
+  volatile int* abort_flag = &S->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&S->full[s]), 1);
+      mbar_init(smem_u32(&S->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&S->tfull[a]), 1);
+      mbar_init(smem_u32(&S->tempty[a]), 4);
+    }
+    mbar_init(smem_u32(&S->drain), 1);
+    S->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&S->tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  pdl_wait();
+  if (threadIdx.x == 0) S->count = read_status(status) != 0 ? 0 : *count_ptr;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  const int nN = (Hp + kBN - 1) / kBN;
+  const long long units = (long long)S->count * nN;
+  const int nk = H / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      uint32_t it = 0;
+      int last_round[kStages];
+      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
+      bool ok = true;
+      for (long long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int4 t = tiles[u / nN];
+        const int n0 = int(u % nN) * kBN;
+        const bool home = t.z < E;
+        const CUtensorMap* wmap = home ? &map_wh : &map_ws;
+        const int wrow = (home ? t.z : t.z - E) * H;
+        const int left = (Hp - n0 + 63) / 64;
+        const int nbox = left < 4 ? left : 4;
+        const uint32_t bytes = kABytes + nbox * kBBox;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = int(it % kStages);
+          const uint32_t round = it / kStages;
+          if (!wait_phase(smem_u32(&S->empty[s]), (round & 1u) ^ 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&S->full[s]);
+          mbar_expect_tx(fb, bytes);
+          tma_load_2d(sa + s * kABytes, &map_x, kb * kBK, t.x, fb);
+          for (int i = 0; i < nbox; ++i)
+            tma_load_2d(sb + s * kBBytes + i * kBBox, wmap, n0 + 64 * i, wrow + kb * kBK, fb);
+          last_round[s] = int(round);
+        }
+      }
+      // wait for this thread's own copies in flight before the CTA may exit
+      for (int s = 0; s < kStages; ++s)
+        if (last_round[s] >= 0)
+          wait_phase(smem_u32(&S->full[s]), uint32_t(last_round[s]) & 1u, abort_flag, status,
+                     false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      uint32_t it = 0, lt = 0;
+      bool ok = true;
+      for (long long u = blockIdx.x; ok && u < units; u += gridDim.x, ++lt) {
+        const uint32_t a = lt & 1u, use = lt >> 1;
+        if (!wait_phase(smem_u32(&S->tempty[a]), (use & 1u) ^ 1u, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + a * kBN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = int(it % kStages);
+          if (!wait_phase(smem_u32(&S->full[s]), (it / kStages) & 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // A: K-major, 16 elements = 32 bytes further along the swizzled row.
+            const uint64_t ad = sdesc(sa + s * kABytes + kk * 32, 16, 1024);
+            // B: MN-major, 16 K rows = 2 groups of 8 rows further down.
+            const uint64_t bd =
+                sdesc(sb + s * kBBytes + kk * 16 * 128, MEP_GEMM_B_LBO, MEP_GEMM_B_SBO);
+            tc_mma(d, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&S->empty[s]));
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&S->tfull[a]));
+      }
+      // every MMA this thread issued has completed once `drain` flips
+      tc_commit(smem_u32(&S->drain));
+      wait_phase(smem_u32(&S->drain), 0u, abort_flag, status, false);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;  // this warp may read TMEM lanes [32q, 32q + 32)
+    uint32_t lt = 0;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
+      const uint32_t a = lt & 1u, use = lt >> 1;
+      if (!wait_phase(smem_u32(&S->tfull[a]), use & 1u, abort_flag, status)) break;
+      tc_fence_after();
+      const int4 t = tiles[u / nN];
+      const int n0 = int(u % nN) * kBN;
+      const int r = 32 * q + lane;
+      const bool row_ok = r < t.y;
+      __nv_bfloat16* out = y + ((long long)t.x + r) * Hp + n0;
+      for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
+        uint32_t v[32];
+        tc_ld32(tmem + a * kBN + 32 * c + ((uint32_t)(32 * q) << 16), v);
+        if (row_ok) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (n0 + 32 * c + 8 * g < Hp) {
+              uint4 o;
+              o.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+              o.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+              o.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+              o.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+              *reinterpret_cast<uint4*>(out + 32 * c + 8 * g) = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S->tempty[a]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 map over a row-major [rows, cols] matrix, box {64 columns, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, unsigned long long rows, unsigned long long cols,
+              unsigned box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+long long max_tiles(int R, int S, int K, int E, int B) {
+  return ((long long)R * S * K + kBM - 1) / kBM + (long long)R * (E + B);
+}
+
+}  // namespace
+}  // namespace mep
+
+using namespace mep;
+
+extern "C" int mep_grouped_gemm_workspace_bytes(int R, int S, int K, int E, int B,
+                                                size_t* bytes) {
+  if (bytes == nullptr || R < 1 || S < 0 || K < 1 || E < 1 || B < 0) return MEP_ERR_INVALID_ARG;
+  if (R > MEP_MAX_R || E > MEP_MAX_E || K > MEP_MAX_K || (long long)R * B > MEP_MAX_SLOTS)
+    return MEP_ERR_INVALID_ARG;
+  *bytes = 16 + 16 * (size_t)max_tiles(R, S, K, E, B);
+  return MEP_OK;
+}
+
+extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
+                                const mep_bf16* w_home, const mep_bf16* w_slot, int32_t* status,
+                                int R, int S, int K, int E, int B, int H, int Hp, void* ws,
+                                size_t ws_bytes, mep_bf16* y, void* stream) {
+  size_t need = 0;
+  if (mep_grouped_gemm_workspace_bytes(R, S, K, E, B, &need) != MEP_OK) return MEP_ERR_INVALID_ARG;
+  if (H < kBK || H % kBK != 0 || Hp < 8 || Hp % 8 != 0) return MEP_ERR_INVALID_ARG;
+  const long long SK = (long long)S * K, rows = (long long)R * SK;
+  if (rows > 0x7fffffffLL || (long long)E * H > 0x7fffffffLL ||
+      (long long)R * B * H > 0x7fffffffLL)
+    return MEP_ERR_INVALID_ARG;
+  if (rows == 0) return MEP_OK;
+  if (x == nullptr || cu_seqlens == nullptr || w_home == nullptr || y == nullptr ||
+      ws == nullptr || ws_bytes < need || (B > 0 && w_slot == nullptr))
+    return MEP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_home) || !aligned16(y) || !aligned16(ws) ||
+      (B > 0 && !aligned16(w_slot)))
+    return MEP_ERR_INVALID_ARG;
+  CUtensorMap mx, mh, msl;
+  if (!make_map(&mx, x, (unsigned long long)rows, (unsigned long long)H, kBM) ||
+      !make_map(&mh, w_home, (unsigned long long)E * H, (unsigned long long)Hp, kBK))
+    return MEP_ERR_CUDA;
+  if (B > 0) {
+    if (!make_map(&msl, w_slot, (unsigned long long)R * B * H, (unsigned long long)Hp, kBK))
+      return MEP_ERR_CUDA;
+  } else {
+    msl = mh;  // never read: every weight row is below E
+  }
+  int* count = static_cast<int*>(ws);
+  int4* tiles = reinterpret_cast<int4*>(static_cast<char*>(ws) + 16);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err = launch_pdl(k_gemm_tiles, dim3(1), dim3(kTileThreads), 0, st, cu_seqlens, R,
+                               E, B, int(SK), status, tiles, count);
+  if (err != cudaSuccess) return MEP_ERR_CUDA;
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm), kSmemBytes)) return MEP_ERR_CUDA;
+  err = launch_pdl(k_gemm, dim3(sm_count()), dim3(kThreads), kSmemBytes, st, mx, mh, msl,
+                   static_cast<const int4*>(tiles), static_cast<const int*>(count), status, E, H,
+                   Hp, reinterpret_cast<__nv_bfloat16*>(y));
+  return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
+}

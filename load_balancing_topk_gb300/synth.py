@@ -249,9 +249,9 @@ def full_slot_map(E: int, R: int, B: int, seed: int = 0) -> np.ndarray:
     raise RuntimeError("could not draw a slot map with no home slots")
 
 
-def integer_valued(shape, seed: int, lo: int = -8, hi: int = 8) -> np.ndarray:
+def integer_valued(shape, seed: int, lo: int = -8, hi: int = 8, tag: int = 99) -> np.ndarray:
     """Small integers stored as float32: sums of these are exact in any order."""
-    g = _rng(seed, 99)
+    g = _rng(seed, tag)
     return g.integers(lo, hi + 1, size=shape).astype(np.float32)
 
 
