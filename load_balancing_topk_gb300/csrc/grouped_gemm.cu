@@ -11,12 +11,20 @@
 //   k_gemm_tiles  (1 CTA) checks every cu_seqlens row and cuts every group
 //                 into 128-row tiles {first buffer row, rows, weight row},
 //                 written to the workspace with their count;
-//   k_gemm        (persistent, one CTA per SM, 192 threads) walks the work
-//                 units (tile, 256-column block of H') grid-stride:
+//   k_gemm        (persistent, one CTA per SM, 192 threads, clusters of
+//                 MEP_GEMM_CLUSTER CTAs) walks the work units (tile, 256-column
+//                 block of H') grid-stride; the CTAs of a cluster take
+//                 adjacent tiles of one group (groups are padded to a whole
+//                 number of tile pairs with empty tiles), so they share the
+//                 weight tile:
 //     warp 0      TMA producer: per 64-wide K step, a 128x64 tile of x
 //                 (K-major, 128-byte swizzle) and up to four 64x64 boxes of
 //                 the weight row (H' contiguous: MN-major, 128-byte swizzle)
-//                 into a 4-stage shared-memory ring;
+//                 into a 4-stage shared-memory ring. In a cluster of 2, each
+//                 CTA loads half of the weight boxes and multicasts them to
+//                 both CTAs, halving the weight traffic out of L2; each MMA
+//                 commit is multicast to both CTAs' stage barriers, so a stage
+//                 is refilled only once both CTAs' MMAs have read it;
 //     warp 1      owns the TMEM allocation (2 x 256 fp32 columns) and, from
 //                 one lane, issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
 //                 fp32 accumulate) and the commits that free ring stages and
@@ -40,6 +48,9 @@
 #endif
 #ifndef MEP_GEMM_B_SBO
 #define MEP_GEMM_B_SBO 1024  // byte stride between 8-row K groups of a weight stage
+#endif
+#ifndef MEP_GEMM_CLUSTER
+#define MEP_GEMM_CLUSTER 2  // CTAs sharing one weight tile (1 or 2)
 #endif
 #ifndef MEP_GEMM_TIMEOUT_NS
 #define MEP_GEMM_TIMEOUT_NS 4000000000ull
@@ -130,6 +141,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same load, landing at the same shared-memory offset (and completing
+// bytes on the mbarrier at the same offset) in every CTA of the cluster
+// named in cta_mask.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -166,6 +199,15 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
+// Arrive on the mbarrier at this offset in every CTA of cta_mask once this
+// thread's MMAs so far have completed.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes, one lane (row)
 // per thread.
@@ -192,8 +234,8 @@ __device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
 // Tile table. tiles[i] = {first buffer row, rows (1..128), weight row, 0}
 // where weight row < E is a home expert and E + r*B + b is slot b of rank r.
 __global__ void __launch_bounds__(kTileThreads)
-    k_gemm_tiles(const int32_t* __restrict__ cu, int R, int E, int B, int SK, int32_t* status,
-                 int4* __restrict__ tiles, int* __restrict__ count) {
+    k_gemm_tiles(const int32_t* __restrict__ cu, int R, int E, int B, int SK, int pair,
+                 int32_t* status, int4* __restrict__ tiles, int* __restrict__ count) {
   pdl_wait();
   pdl_launch_dependents();
   __shared__ int s_warp[33];
@@ -234,16 +276,20 @@ __global__ void __launch_bounds__(kTileThreads)
       lo = j == 0 ? 0 : cu[p - 1];
       len = cu[p] - lo;
     }
-    s_nt[threadIdx.x] = (len + kBM - 1) / kBM;
+    const int nt = (len + kBM - 1) / kBM;
+    s_nt[threadIdx.x] = (nt + pair - 1) / pair * pair;  // empty tiles complete the last pair
     __syncthreads();
     block_excl_scan(s_nt, s_nt, blockDim.x, s_warp, true);
     if (p < RG && len > 0) {
       const int r = int(p / G), j = int(p % G);
       const int widx = j < E ? j : E + r * B + (j - E);
       const long long row0 = (long long)r * SK + lo;
-      int off = s_carry + s_nt[threadIdx.x];
-      for (int m = 0; m * kBM < len; ++m, ++off)
-        tiles[off] = make_int4(int(row0 + (long long)m * kBM), min(kBM, len - m * kBM), widx, 0);
+      const int off = s_carry + s_nt[threadIdx.x];
+      const int nt = (len + kBM - 1) / kBM;
+      const int padded = (nt + pair - 1) / pair * pair;
+      for (int m = 0; m < padded; ++m)
+        tiles[off + m] = make_int4(int(row0 + (long long)m * kBM), max(0, min(kBM, len - m * kBM)),
+                                   widx, 0);
     }
     __syncthreads();
     if (threadIdx.x == 0) s_carry += s_nt[blockDim.x];
@@ -260,11 +306,14 @@ struct GemmSmem {
   int count;
 };
 
+template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wh,
            const __grid_constant__ CUtensorMap map_ws, const int4* __restrict__ tiles,
            const int* __restrict__ count_ptr, int32_t* status, int E, int H, int Hp,
            __nv_bfloat16* __restrict__ y) {
+  static_assert(CL == 1 || CL == 2, "clusters of 1 or 2 CTAs");
+  constexpr uint16_t kMask = (1u << CL) - 1u;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzled stages want 1024-byte alignment
@@ -275,10 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &S->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CL > 1 ? int(cluster_rank()) : 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&S->full[s]), 1);
-      mbar_init(smem_u32(&S->empty[s]), 1);
+      mbar_init(smem_u32(&S->empty[s]), CL);  // one MMA commit from every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&S->tfull[a]), 1);
@@ -300,10 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) S->count = read_status(status) != 0 ? 0 : *count_ptr;
   tc_fence_before();
   __syncthreads();
+  // the peer multicasts into this CTA's ring only after its barriers exist
+  if (CL > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = S->tmem;
   const int nN = (Hp + kBN - 1) / kBN;
-  const long long units = (long long)S->count * nN;
+  // work units of the cluster: (pair of adjacent tiles, column block); CTA
+  // `rank` of the cluster takes tile CL * pair + rank
+  const long long units = (long long)(S->count / CL) * nN;
+  const long long u0 = blockIdx.x / CL, ustep = gridDim.x / CL;
   const int nk = H / kBK;
 
   if (warp == 0) {
@@ -313,15 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_round[kStages];
       for (int s = 0; s < kStages; ++s) last_round[s] = -1;
       bool ok = true;
-      for (long long u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const int4 t = tiles[u / nN];
+      for (long long u = u0; ok && u < units; u += ustep) {
+        const int4 t = tiles[(u / nN) * CL + rank];
         const int n0 = int(u % nN) * kBN;
         const bool home = t.z < E;
         const CUtensorMap* wmap = home ? &map_wh : &map_ws;
         const int wrow = (home ? t.z : t.z - E) * H;
         const int left = (Hp - n0 + 63) / 64;
         const int nbox = left < 4 ? left : 4;
-        const uint32_t bytes = kABytes + nbox * kBBox;
+        const uint32_t bytes = kABytes + nbox * kBBox;  // every box lands in every CTA
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = int(it % kStages);
           const uint32_t round = it / kStages;
@@ -332,16 +387,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&S->full[s]);
           mbar_expect_tx(fb, bytes);
           tma_load_2d(sa + s * kABytes, &map_x, kb * kBK, t.x, fb);
-          for (int i = 0; i < nbox; ++i)
-            tma_load_2d(sb + s * kBBytes + i * kBBox, wmap, n0 + 64 * i, wrow + kb * kBK, fb);
+          for (int i = rank; i < nbox; i += CL) {
+            if (CL > 1)
+              tma_load_2d_mc(sb + s * kBBytes + i * kBBox, wmap, n0 + 64 * i, wrow + kb * kBK, fb,
+                             kMask);
+            else
+              tma_load_2d(sb + s * kBBytes + i * kBBox, wmap, n0 + 64 * i, wrow + kb * kBK, fb);
+          }
           last_round[s] = int(round);
         }
       }
-      // wait for this thread's own copies in flight before the CTA may exit
+      // before the CTA may exit: its ring has received every copy it asked
+      // for, and (cluster) every MMA commit aimed at its stage barriers
       for (int s = 0; s < kStages; ++s)
-        if (last_round[s] >= 0)
+        if (last_round[s] >= 0) {
           wait_phase(smem_u32(&S->full[s]), uint32_t(last_round[s]) & 1u, abort_flag, status,
                      false);
+          if (CL > 1)
+            wait_phase(smem_u32(&S->empty[s]), uint32_t(last_round[s]) & 1u, abort_flag, status,
+                       false);
+        }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -349,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- MMA issuer ----------------
       uint32_t it = 0, lt = 0;
       bool ok = true;
-      for (long long u = blockIdx.x; ok && u < units; u += gridDim.x, ++lt) {
+      for (long long u = u0; ok && u < units; u += ustep, ++lt) {
         const uint32_t a = lt & 1u, use = lt >> 1;
         if (!wait_phase(smem_u32(&S->tempty[a]), (use & 1u) ^ 1u, abort_flag, status)) break;
         tc_fence_after();
@@ -370,7 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sdesc(sb + s * kBBytes + kk * 16 * 128, MEP_GEMM_B_LBO, MEP_GEMM_B_SBO);
             tc_mma(d, ad, bd, (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(&S->empty[s]));
+          // the stage is free in every CTA of the cluster once all their MMAs read it
+          if (CL > 1)
+            tc_commit_mc(smem_u32(&S->empty[s]), kMask);
+          else
+            tc_commit(smem_u32(&S->empty[s]));
         }
         if (!ok) break;
         tc_commit(smem_u32(&S->tfull[a]));
@@ -384,14 +453,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;  // this warp may read TMEM lanes [32q, 32q + 32)
     uint32_t lt = 0;
-    for (long long u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
+    for (long long u = u0; u < units; u += ustep, ++lt) {
       const uint32_t a = lt & 1u, use = lt >> 1;
       if (!wait_phase(smem_u32(&S->tfull[a]), use & 1u, abort_flag, status)) break;
       tc_fence_after();
-      const int4 t = tiles[u / nN];
+      const int4 t = tiles[(u / nN) * CL + rank];
       const int n0 = int(u % nN) * kBN;
       const int r = 32 * q + lane;
-      const bool row_ok = r < t.y;
+      const bool row_ok = r < t.y;  // padding tiles have no rows
       __nv_bfloat16* out = y + ((long long)t.x + r) * Hp + n0;
       for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
         uint32_t v[32];
@@ -417,6 +486,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) {
+    cluster_sync();
+    // After an error (a wait that gave up), a peer's copy or commit may still
+    // be in flight towards this CTA: give it time to land before either exits.
+    if (threadIdx.x == 0 && read_status(status) != 0) {
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 100000ull) {
+      }
+    }
+    cluster_sync();
+  }
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -460,8 +540,45 @@ bool make_map(CUtensorMap* m, const void* ptr, unsigned long long rows, unsigned
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Each group adds at most one partial tile and one padding tile.
 long long max_tiles(int R, int S, int K, int E, int B) {
-  return ((long long)R * S * K + kBM - 1) / kBM + (long long)R * (E + B);
+  return ((long long)R * S * K + kBM - 1) / kBM + 2LL * R * (E + B);
+}
+
+// Launch k_gemm<CL> as a persistent grid: as many clusters as can be
+// resident at once (a cluster of 2 needs two free SMs of one GPC), found
+// once per device and cached.
+template <int CL>
+cudaError_t launch_gemm(cudaStream_t st, const CUtensorMap& mx, const CUtensorMap& mh,
+                        const CUtensorMap& msl, const int4* tiles, const int* count,
+                        int32_t* status, int E, int H, int Hp, __nv_bfloat16* y) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  static int cached_dev = -1, cached_grid = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev != cached_dev) {
+    int nclusters = 0;
+    cfg.gridDim = dim3(sm_count() / CL * CL);
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, k_gemm<CL>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (nclusters < 1) return cudaErrorInvalidConfiguration;
+    cached_grid = (nclusters * CL < sm_count() ? nclusters : sm_count() / CL) * CL;
+    cached_dev = dev;
+  }
+  cfg.gridDim = dim3(cached_grid);
+  return cudaLaunchKernelEx(&cfg, k_gemm<CL>, mx, mh, msl, tiles, count, status, E, H, Hp, y);
 }
 
 }  // namespace
@@ -486,7 +603,7 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
   if (mep_grouped_gemm_workspace_bytes(R, S, K, E, B, &need) != MEP_OK) return MEP_ERR_INVALID_ARG;
   if (H < kBK || H % kBK != 0 || Hp < 8 || Hp % 8 != 0) return MEP_ERR_INVALID_ARG;
   const long long SK = (long long)S * K, rows = (long long)R * SK;
-  if (rows > 0x7fffffffLL || (long long)E * H > 0x7fffffffLL ||
+  if (rows > 0x7fffff00LL || (long long)E * H > 0x7fffffffLL ||
       (long long)R * B * H > 0x7fffffffLL)
     return MEP_ERR_INVALID_ARG;
   if (rows == 0) return MEP_OK;
@@ -509,12 +626,13 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
   int* count = static_cast<int*>(ws);
   int4* tiles = reinterpret_cast<int4*>(static_cast<char*>(ws) + 16);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  constexpr int CL = MEP_GEMM_CLUSTER;
   cudaError_t err = launch_pdl(k_gemm_tiles, dim3(1), dim3(kTileThreads), 0, st, cu_seqlens, R,
-                               E, B, int(SK), status, tiles, count);
+                               E, B, int(SK), CL, status, tiles, count);
   if (err != cudaSuccess) return MEP_ERR_CUDA;
-  if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm), kSmemBytes)) return MEP_ERR_CUDA;
-  err = launch_pdl(k_gemm, dim3(sm_count()), dim3(kThreads), kSmemBytes, st, mx, mh, msl,
-                   static_cast<const int4*>(tiles), static_cast<const int*>(count), status, E, H,
-                   Hp, reinterpret_cast<__nv_bfloat16*>(y));
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm<CL>), kSmemBytes))
+    return MEP_ERR_CUDA;
+  err = launch_gemm<CL>(st, mx, mh, msl, tiles, count, status, E, H, Hp,
+                        reinterpret_cast<__nv_bfloat16*>(y));
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
