@@ -52,6 +52,9 @@
 #ifndef MEP_GEMM_CLUSTER
 #define MEP_GEMM_CLUSTER 2  // CTAs sharing one weight tile (1 or 2)
 #endif
+#ifndef MEP_GEMM_PAIR_MMA
+#define MEP_GEMM_PAIR_MMA 1  // clusters of 2 run k_gemm_pair (cta_group::2 MMAs)
+#endif
 #ifndef MEP_GEMM_TIMEOUT_NS
 #define MEP_GEMM_TIMEOUT_NS 4000000000ull
 #endif
@@ -153,6 +156,27 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* 
       : "memory");
 }
 
+// cta_group::2 form: the data lands in this CTA's shared memory, the bytes
+// are counted on an mbarrier that may sit in the peer CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -206,6 +230,33 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
+      : "memory");
+}
+
+// The pair form: M = 256 rows over the two CTAs of a pair (each CTA's 128
+// rows of A and 128 of the 256 columns of B in its own shared memory, each
+// CTA's 128 rows of D in its own TMEM), issued by one thread of CTA 0.
+constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                             ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+__device__ __forceinline__ void tc_mma2(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc2), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit2_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit2(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
 
@@ -299,8 +350,9 @@ __global__ void __launch_bounds__(kTileThreads)
 }
 
 // ---------------------------------------------------------------------------
+constexpr int kStages2 = 6;  // ring depth of the CTA-pair kernel (32 KB stages)
 struct GemmSmem {
-  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain;
+  uint64_t full[kStages2], empty[kStages2], tfull[2], tempty[2], drain;
   uint32_t tmem;
   int abort;
   int count;
@@ -505,6 +557,194 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// CTA-pair kernel (cta_group::2). Clusters of two CTAs, as in k_gemm<2>: CTA
+// r of the pair takes tile 2p + r of a pair of adjacent tiles of one group.
+// Each CTA stages its own 128x64 x tile and its half (128 columns) of the
+// 256-column weight tile, so a stage is 32 KB per CTA and the ring is 6
+// deep. Both CTAs' copies count on CTA 0's `full` barrier; one thread of CTA
+// 0 issues the M=256 MMAs and multicasts every commit to both CTAs (stage
+// free, accumulator ready). CTA 1's epilogue warps release an accumulator by
+// arriving on CTA 0's `tempty` barrier (8 arrivals: 4 warps per CTA).
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wh,
+                const __grid_constant__ CUtensorMap map_ws, const int4* __restrict__ tiles,
+                const int* __restrict__ count_ptr, int32_t* status, int E, int H, int Hp,
+                __nv_bfloat16* __restrict__ y) {
+  constexpr int kSt = kStages2;
+  constexpr int kBHalf = 2 * kBBox;  // 128 weight columns per CTA per stage
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gen_base = smem_raw + (base - raw);
+  const uint32_t sa = base;
+  const uint32_t sb = base + kSt * kABytes;
+  GemmSmem* S = reinterpret_cast<GemmSmem*>(gen_base + kSt * (kABytes + kBHalf));
+  volatile int* abort_flag = &S->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = int(cluster_rank());
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSt; ++s) {
+      mbar_init(smem_u32(&S->full[s]), 1);   // CTA 0: its producer's arrive + both CTAs' bytes
+      mbar_init(smem_u32(&S->empty[s]), 1);  // CTA 0's multicast commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&S->tfull[a]), 1);
+      mbar_init(smem_u32(&S->tempty[a]), 8);
+    }
+    mbar_init(smem_u32(&S->drain), 1);
+    S->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {  // one warp of each CTA allocates the pair's TMEM together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&S->tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  pdl_wait();
+  if (threadIdx.x == 0) S->count = read_status(status) != 0 ? 0 : *count_ptr;
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  const int nN = (Hp + kBN - 1) / kBN;
+  const long long units = (long long)(S->count / 2) * nN;
+  const long long u0 = blockIdx.x / 2, ustep = gridDim.x / 2;
+  const int nk = H / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      uint32_t it = 0;
+      int last_round[kSt];
+      for (int s = 0; s < kSt; ++s) last_round[s] = -1;
+      bool ok = true;
+      for (long long u = u0; ok && u < units; u += ustep) {
+        const int4 t = tiles[(u / nN) * 2 + rank];
+        const int n0 = int(u % nN) * kBN;
+        const bool home = t.z < E;
+        const CUtensorMap* wmap = home ? &map_wh : &map_ws;
+        const int wrow = (home ? t.z : t.z - E) * H;
+        const int left = (Hp - n0 + 63) / 64;
+        const int nbox = left < 4 ? left : 4;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = int(it % kSt);
+          const uint32_t round = it / kSt;
+          if (!wait_phase(smem_u32(&S->empty[s]), (round & 1u) ^ 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb0 = map_to_rank(smem_u32(&S->full[s]), 0);
+          if (leader) mbar_expect_tx(smem_u32(&S->full[s]), 2 * kABytes + nbox * kBBox);
+          tma_load_2d_pair(sa + s * kABytes, &map_x, kb * kBK, t.x, fb0);
+          for (int i = 2 * rank; i < nbox && i < 2 * rank + 2; ++i)
+            tma_load_2d_pair(sb + s * kBHalf + (i - 2 * rank) * kBBox, wmap, n0 + 64 * i,
+                             wrow + kb * kBK, fb0);
+          last_round[s] = int(round);
+        }
+      }
+      // CTA 0: every copy of both CTAs has landed; both: every commit aimed
+      // at this CTA's stage barriers has arrived
+      for (int s = 0; s < kSt; ++s)
+        if (last_round[s] >= 0) {
+          if (leader)
+            wait_phase(smem_u32(&S->full[s]), uint32_t(last_round[s]) & 1u, abort_flag, status,
+                       false);
+          wait_phase(smem_u32(&S->empty[s]), uint32_t(last_round[s]) & 1u, abort_flag, status,
+                     false);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (CTA 0 only) ----------------
+      uint32_t it = 0, lt = 0;
+      bool ok = true;
+      for (long long u = u0; ok && u < units; u += ustep, ++lt) {
+        const uint32_t a = lt & 1u, use = lt >> 1;
+        if (!wait_phase(smem_u32(&S->tempty[a]), (use & 1u) ^ 1u, abort_flag, status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + a * kBN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = int(it % kSt);
+          if (!wait_phase(smem_u32(&S->full[s]), (it / kSt) & 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = sdesc(sa + s * kABytes + kk * 32, 16, 1024);
+            const uint64_t bd =
+                sdesc(sb + s * kBHalf + kk * 16 * 128, MEP_GEMM_B_LBO, MEP_GEMM_B_SBO);
+            tc_mma2(d, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit2_mc(smem_u32(&S->empty[s]), 3);
+        }
+        if (!ok) break;
+        tc_commit2_mc(smem_u32(&S->tfull[a]), 3);
+      }
+      tc_commit2(smem_u32(&S->drain));
+      wait_phase(smem_u32(&S->drain), 0u, abort_flag, status, false);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
+    const int q = warp & 3;
+    uint32_t lt = 0;
+    for (long long u = u0; u < units; u += ustep, ++lt) {
+      const uint32_t a = lt & 1u, use = lt >> 1;
+      if (!wait_phase(smem_u32(&S->tfull[a]), use & 1u, abort_flag, status)) break;
+      tc_fence_after();
+      const int4 t = tiles[(u / nN) * 2 + rank];
+      const int n0 = int(u % nN) * kBN;
+      const int r = 32 * q + lane;
+      const bool row_ok = r < t.y;
+      __nv_bfloat16* out = y + ((long long)t.x + r) * Hp + n0;
+      for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
+        uint32_t v[32];
+        tc_ld32(tmem + a * kBN + 32 * c + ((uint32_t)(32 * q) << 16), v);
+        if (row_ok) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (n0 + 32 * c + 8 * g < Hp) {
+              uint4 o;
+              o.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+              o.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+              o.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+              o.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+              *reinterpret_cast<uint4*>(out + 32 * c + 8 * g) = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&S->tempty[a]), 0));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (threadIdx.x == 0 && read_status(status) != 0) {
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 100000ull) {
+    }
+  }
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -545,13 +785,14 @@ long long max_tiles(int R, int S, int K, int E, int B) {
   return ((long long)R * S * K + kBM - 1) / kBM + 2LL * R * (E + B);
 }
 
-// Launch k_gemm<CL> as a persistent grid: as many clusters as can be
-// resident at once (a cluster of 2 needs two free SMs of one GPC), found
-// once per device and cached.
-template <int CL>
-cudaError_t launch_gemm(cudaStream_t st, const CUtensorMap& mx, const CUtensorMap& mh,
-                        const CUtensorMap& msl, const int4* tiles, const int* count,
-                        int32_t* status, int E, int H, int Hp, __nv_bfloat16* y) {
+// Launch a GEMM kernel as a persistent grid of clusters of CL CTAs: as many
+// clusters as can be resident at once (a cluster of 2 needs two free SMs of
+// one GPC), found once per device and kernel and cached by the caller.
+template <typename Kernel>
+cudaError_t launch_gemm(Kernel kernel, int CL, int* cached_dev, int* cached_grid, cudaStream_t st,
+                        const CUtensorMap& mx, const CUtensorMap& mh, const CUtensorMap& msl,
+                        const int4* tiles, const int* count, int32_t* status, int E, int H,
+                        int Hp, __nv_bfloat16* y) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -565,20 +806,19 @@ cudaError_t launch_gemm(cudaStream_t st, const CUtensorMap& mx, const CUtensorMa
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  static int cached_dev = -1, cached_grid = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (dev != cached_dev) {
+  if (dev != *cached_dev) {
     int nclusters = 0;
     cfg.gridDim = dim3(sm_count() / CL * CL);
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, k_gemm<CL>, &cfg);
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, kernel, &cfg);
     if (e != cudaSuccess) return e;
     if (nclusters < 1) return cudaErrorInvalidConfiguration;
-    cached_grid = (nclusters * CL < sm_count() ? nclusters : sm_count() / CL) * CL;
-    cached_dev = dev;
+    *cached_grid = (nclusters * CL < sm_count() ? nclusters : sm_count() / CL) * CL;
+    *cached_dev = dev;
   }
-  cfg.gridDim = dim3(cached_grid);
-  return cudaLaunchKernelEx(&cfg, k_gemm<CL>, mx, mh, msl, tiles, count, status, E, H, Hp, y);
+  cfg.gridDim = dim3(*cached_grid);
+  return cudaLaunchKernelEx(&cfg, kernel, mx, mh, msl, tiles, count, status, E, H, Hp, y);
 }
 
 }  // namespace
@@ -630,9 +870,19 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
   cudaError_t err = launch_pdl(k_gemm_tiles, dim3(1), dim3(kTileThreads), 0, st, cu_seqlens, R,
                                E, B, int(SK), CL, status, tiles, count);
   if (err != cudaSuccess) return MEP_ERR_CUDA;
-  if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm<CL>), kSmemBytes))
-    return MEP_ERR_CUDA;
-  err = launch_gemm<CL>(st, mx, mh, msl, tiles, count, status, E, H, Hp,
-                        reinterpret_cast<__nv_bfloat16*>(y));
+  __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(y);
+  if (CL == 2 && MEP_GEMM_PAIR_MMA) {
+    static int dev_cache = -1, grid_cache = 0;
+    if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm_pair), kSmemBytes))
+      return MEP_ERR_CUDA;
+    err = launch_gemm(k_gemm_pair, 2, &dev_cache, &grid_cache, st, mx, mh, msl, tiles, count,
+                      status, E, H, Hp, yb);
+  } else {
+    static int dev_cache = -1, grid_cache = 0;
+    if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm<CL>), kSmemBytes))
+      return MEP_ERR_CUDA;
+    err = launch_gemm(k_gemm<CL>, CL, &dev_cache, &grid_cache, st, mx, mh, msl, tiles, count,
+                      status, E, H, Hp, yb);
+  }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
