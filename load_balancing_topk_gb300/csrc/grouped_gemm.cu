@@ -10,29 +10,32 @@
 // Two launches on the caller's stream:
 //   k_gemm_tiles  (1 CTA) checks every cu_seqlens row and cuts every group
 //                 into 128-row tiles {first buffer row, rows, weight row},
+//                 padded with empty tiles to a whole number of pairs,
 //                 written to the workspace with their count;
-//   k_gemm        (persistent, one CTA per SM, 192 threads, clusters of
-//                 MEP_GEMM_CLUSTER CTAs) walks the work units (tile, 256-column
-//                 block of H') grid-stride; the CTAs of a cluster take
-//                 adjacent tiles of one group (groups are padded to a whole
-//                 number of tile pairs with empty tiles), so they share the
-//                 weight tile:
-//     warp 0      TMA producer: per 64-wide K step, a 128x64 tile of x
-//                 (K-major, 128-byte swizzle) and up to four 64x64 boxes of
-//                 the weight row (H' contiguous: MN-major, 128-byte swizzle)
-//                 into a 4-stage shared-memory ring. In a cluster of 2, each
-//                 CTA loads half of the weight boxes and multicasts them to
-//                 both CTAs, halving the weight traffic out of L2; each MMA
-//                 commit is multicast to both CTAs' stage barriers, so a stage
-//                 is refilled only once both CTAs' MMAs have read it;
-//     warp 1      owns the TMEM allocation (2 x 256 fp32 columns) and, from
-//                 one lane, issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
-//                 fp32 accumulate) and the commits that free ring stages and
-//                 hand finished accumulators to the epilogue;
-//     warps 2..5  epilogue: tcgen05.ld of their 32 TMEM lanes (= tile rows),
-//                 round to bf16 (nearest-even) and store the valid rows and
-//                 columns; the accumulator is double-buffered, so the next
-//                 unit's MMAs overlap this store.
+//   k_gemm_pair   (default) persistent clusters of two CTAs, one per SM, 192
+//                 threads each, over the work units (pair of adjacent tiles
+//                 of one group, 256-column block of H'), grid-stride:
+//     warp 0      TMA producer of each CTA: per 64-wide K step, its own
+//                 128x64 tile of x (K-major, 128-byte swizzle) and its half
+//                 (two 64x64 boxes) of the weight row's 256 columns (H'
+//                 contiguous: MN-major, 128-byte swizzle) into a 6-stage
+//                 ring; both CTAs' copies count on CTA 0's stage barrier;
+//     warp 1      allocates the pair's TMEM (2 x 256 fp32 columns in each
+//                 CTA, cta_group::2) and, in CTA 0, issues from one lane the
+//                 pair MMAs (tcgen05.mma.cta_group::2: M = 256 over the two
+//                 CTAs, N = 256, K = 16, bf16 in, fp32 accumulate); every
+//                 commit is multicast to both CTAs (stage free, accumulator
+//                 ready);
+//     warps 2..5  epilogue of each CTA: tcgen05.ld of its 128 TMEM lanes
+//                 (= its tile's rows), bf16 (nearest-even), stores of the
+//                 valid rows and columns, then a release on CTA 0's
+//                 accumulator barrier; the accumulator is double-buffered,
+//                 so the next unit's MMAs overlap this store.
+//   k_gemm<CL>    the same pipeline with 1-SM MMAs (M = 128): for CL = 2 the
+//                 two CTAs of a cluster share the weight tile by TMA
+//                 multicast (4-stage ring of 48 KB); for CL = 1 every CTA
+//                 loads its own. Selected by MEP_GEMM_PAIR_MMA=0 or
+//                 MEP_GEMM_CLUSTER=1 at build time.
 // Every wait is bounded (MEP_GEMM_TIMEOUT_NS on %globaltimer): a wait that
 // gives up raises a CTA-wide abort flag and MEP_ERR_TIMEOUT; every role then
 // leaves its loop, the producer waits for its own copies in flight, the MMA
