@@ -18,8 +18,9 @@
 //     warp 0      TMA producer of each CTA: per 64-wide K step, its own
 //                 128x64 tile of x (K-major, 128-byte swizzle) and its half
 //                 (two 64x64 boxes) of the weight row's 256 columns (H'
-//                 contiguous: MN-major, 128-byte swizzle) into a 6-stage
-//                 ring; both CTAs' copies count on CTA 0's stage barrier;
+//                 contiguous: MN-major, 128-byte swizzle) into a ring of
+//                 MEP_GEMM_PAIR_STAGES 32 KB stages; both CTAs' copies count
+//                 on CTA 0's stage barrier;
 //     warp 1      allocates the pair's TMEM (2 x 256 fp32 columns in each
 //                 CTA, cta_group::2) and, in CTA 0, issues from one lane the
 //                 pair MMAs (tcgen05.mma.cta_group::2: M = 256 over the two
@@ -27,8 +28,8 @@
 //                 commit is multicast to both CTAs (stage free, accumulator
 //                 ready);
 //     warps 2..5  epilogue of each CTA: tcgen05.ld of its 128 TMEM lanes
-//                 (= its tile's rows), bf16 (nearest-even), stores of the
-//                 valid rows and columns, then a release on CTA 0's
+//                 (= its tile's rows), bf16 (nearest-even), whole-sector
+//                 stores of the valid rows and columns, then a release on CTA 0's
 //                 accumulator barrier; the accumulator is double-buffered,
 //                 so the next unit's MMAs overlap this store.
 //   k_gemm<CL>    the same pipeline with 1-SM MMAs (M = 128): for CL = 2 the
@@ -57,6 +58,9 @@
 #endif
 #ifndef MEP_GEMM_PAIR_MMA
 #define MEP_GEMM_PAIR_MMA 1  // clusters of 2 run k_gemm_pair (cta_group::2 MMAs)
+#endif
+#ifndef MEP_GEMM_ST32
+#define MEP_GEMM_ST32 1  // epilogue stores whole 32-byte sectors when H' % 16 == 0
 #endif
 #ifndef MEP_GEMM_TIMEOUT_NS
 #define MEP_GEMM_TIMEOUT_NS 4000000000ull
@@ -284,6 +288,32 @@ __device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// 32 fp32 accumulator columns of one row -> bf16 (nearest-even) at out[0..32),
+// columns at or beyond `left` skipped. st32: whole 32-byte sectors per store
+// (needs H' % 16 == 0 and a 32-byte aligned y, checked on the host), else
+// 16-byte stores (H' % 8 == 0).
+__device__ __forceinline__ void store_chunk(__nv_bfloat16* out, const uint32_t (&v)[32], int left,
+                                            bool st32) {
+  uint32_t o[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j] = pack_bf16(v[2 * j], v[2 * j + 1]);
+  if (st32) {
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+      if (16 * g < left)
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(out + 16 * g),
+                     "r"(o[8 * g + 0]), "r"(o[8 * g + 1]), "r"(o[8 * g + 2]), "r"(o[8 * g + 3]),
+                     "r"(o[8 * g + 4]), "r"(o[8 * g + 5]), "r"(o[8 * g + 6]), "r"(o[8 * g + 7])
+                     : "memory");
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (8 * g < left)
+        *reinterpret_cast<uint4*>(out + 8 * g) =
+            make_uint4(o[4 * g + 0], o[4 * g + 1], o[4 * g + 2], o[4 * g + 3]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Tile table. tiles[i] = {first buffer row, rows (1..128), weight row, 0}
 // where weight row < E is a home expert and E + r*B + b is slot b of rank r.
@@ -353,7 +383,12 @@ __global__ void __launch_bounds__(kTileThreads)
 }
 
 // ---------------------------------------------------------------------------
-constexpr int kStages2 = 6;  // ring depth of the CTA-pair kernel (32 KB stages)
+#ifndef MEP_GEMM_PAIR_STAGES
+#define MEP_GEMM_PAIR_STAGES 5
+#endif
+constexpr int kStages2 = MEP_GEMM_PAIR_STAGES;  // ring depth of the CTA-pair kernel (32 KB stages)
+constexpr int kSmemPair = 1024 /* alignment slack */ + kStages2 * (kABytes + 2 * kBBox) + 256;
+static_assert(kSmemPair <= 232448, "the CTA-pair ring must fit in 227 KB of shared memory");
 struct GemmSmem {
   uint64_t full[kStages2], empty[kStages2], tfull[2], tempty[2], drain;
   uint32_t tmem;
@@ -366,8 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wh,
            const __grid_constant__ CUtensorMap map_ws, const int4* __restrict__ tiles,
            const int* __restrict__ count_ptr, int32_t* status, int E, int H, int Hp,
-           __nv_bfloat16* __restrict__ y) {
+           __nv_bfloat16* __restrict__ y, int st32_flag) {
   static_assert(CL == 1 || CL == 2, "clusters of 1 or 2 CTAs");
+  const bool st32 = st32_flag != 0;
   constexpr uint16_t kMask = (1u << CL) - 1u;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -520,19 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
         uint32_t v[32];
         tc_ld32(tmem + a * kBN + 32 * c + ((uint32_t)(32 * q) << 16), v);
-        if (row_ok) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (n0 + 32 * c + 8 * g < Hp) {
-              uint4 o;
-              o.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
-              o.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
-              o.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
-              o.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
-              *reinterpret_cast<uint4*>(out + 32 * c + 8 * g) = o;
-            }
-          }
-        }
+        if (row_ok) store_chunk(out + 32 * c, v, Hp - (n0 + 32 * c), st32);
       }
       tc_fence_before();
       __syncwarp();
@@ -572,8 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wh,
                 const __grid_constant__ CUtensorMap map_ws, const int4* __restrict__ tiles,
                 const int* __restrict__ count_ptr, int32_t* status, int E, int H, int Hp,
-                __nv_bfloat16* __restrict__ y) {
+                __nv_bfloat16* __restrict__ y, int st32_flag) {
   constexpr int kSt = kStages2;
+  const bool st32 = st32_flag != 0;
   constexpr int kBHalf = 2 * kBBox;  // 128 weight columns per CTA per stage
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -712,19 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
         uint32_t v[32];
         tc_ld32(tmem + a * kBN + 32 * c + ((uint32_t)(32 * q) << 16), v);
-        if (row_ok) {
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (n0 + 32 * c + 8 * g < Hp) {
-              uint4 o;
-              o.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
-              o.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
-              o.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
-              o.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
-              *reinterpret_cast<uint4*>(out + 32 * c + 8 * g) = o;
-            }
-          }
-        }
+        if (row_ok) store_chunk(out + 32 * c, v, Hp - (n0 + 32 * c), st32);
       }
       tc_fence_before();
       __syncwarp();
@@ -792,10 +805,11 @@ long long max_tiles(int R, int S, int K, int E, int B) {
 // clusters as can be resident at once (a cluster of 2 needs two free SMs of
 // one GPC), found once per device and kernel and cached by the caller.
 template <typename Kernel>
-cudaError_t launch_gemm(Kernel kernel, int CL, int* cached_dev, int* cached_grid, cudaStream_t st,
+cudaError_t launch_gemm(Kernel kernel, int CL, int smem, int* cached_dev, int* cached_grid,
+                        cudaStream_t st,
                         const CUtensorMap& mx, const CUtensorMap& mh, const CUtensorMap& msl,
                         const int4* tiles, const int* count, int32_t* status, int E, int H,
-                        int Hp, __nv_bfloat16* y) {
+                        int Hp, __nv_bfloat16* y, int st32) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -805,7 +819,7 @@ cudaError_t launch_gemm(Kernel kernel, int CL, int* cached_dev, int* cached_grid
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
@@ -821,7 +835,7 @@ cudaError_t launch_gemm(Kernel kernel, int CL, int* cached_dev, int* cached_grid
     *cached_dev = dev;
   }
   cfg.gridDim = dim3(*cached_grid);
-  return cudaLaunchKernelEx(&cfg, kernel, mx, mh, msl, tiles, count, status, E, H, Hp, y);
+  return cudaLaunchKernelEx(&cfg, kernel, mx, mh, msl, tiles, count, status, E, H, Hp, y, st32);
 }
 
 }  // namespace
@@ -874,18 +888,20 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
                                E, B, int(SK), CL, status, tiles, count);
   if (err != cudaSuccess) return MEP_ERR_CUDA;
   __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(y);
+  const int st32 =
+      MEP_GEMM_ST32 && Hp % 16 == 0 && (reinterpret_cast<uintptr_t>(y) & 31u) == 0 ? 1 : 0;
   if (CL == 2 && MEP_GEMM_PAIR_MMA) {
     static int dev_cache = -1, grid_cache = 0;
-    if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm_pair), kSmemBytes))
+    if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm_pair), kSmemPair))
       return MEP_ERR_CUDA;
-    err = launch_gemm(k_gemm_pair, 2, &dev_cache, &grid_cache, st, mx, mh, msl, tiles, count,
-                      status, E, H, Hp, yb);
+    err = launch_gemm(k_gemm_pair, 2, kSmemPair, &dev_cache, &grid_cache, st, mx, mh, msl, tiles,
+                      count, status, E, H, Hp, yb, st32);
   } else {
     static int dev_cache = -1, grid_cache = 0;
     if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm<CL>), kSmemBytes))
       return MEP_ERR_CUDA;
-    err = launch_gemm(k_gemm<CL>, CL, &dev_cache, &grid_cache, st, mx, mh, msl, tiles, count,
-                      status, E, H, Hp, yb);
+    err = launch_gemm(k_gemm<CL>, CL, kSmemBytes, &dev_cache, &grid_cache, st, mx, mh, msl,
+                      tiles, count, status, E, H, Hp, yb, st32);
   }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
