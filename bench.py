@@ -339,6 +339,32 @@ def gpu_arm(args, rank: int, world: int, dist):
     h2d = idx.nbytes + w.nbytes + x_np.nbytes
     d2h = s.N * s.H * 2 + 4
 
+    def copies_only(reps=5):
+        """The same per-step copies, both directions at once, no compute:
+        the host-link bound of the end-to-end step."""
+        b = sets[0]
+        ts = []
+        for r in range(reps + 1):
+            e0, e_in, e_out = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            torch.cuda.synchronize()
+            e0.record(s_in)
+            s_out.wait_event(e0)
+            with torch.cuda.stream(s_in):
+                b["idx"].copy_(idx_h, non_blocking=True)
+                b["w"].copy_(w_h, non_blocking=True)
+                b["x"].copy_(x_h, non_blocking=True)
+                e_in.record(s_in)
+            with torch.cuda.stream(s_out):
+                b["out_h"].copy_(b["out"], non_blocking=True)
+                b["st_h"].copy_(plan.status, non_blocking=True)
+                e_out.record(s_out)
+            torch.cuda.synchronize()
+            if r:
+                ts.append(max(e0.elapsed_time(e_in), e0.elapsed_time(e_out)))
+        return float(np.median(ts))
+
+    link_ms = copies_only()
+
     sweep = run_sweep(args, dev, rank) if (args.sweep and rank == 0) else None
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
@@ -348,7 +374,7 @@ def gpu_arm(args, rank: int, world: int, dist):
     res = dict(
         next_rows=nxt,
         total_ms=t_max, steps=args.steps, total_bytes=total_bytes, nb=nb, times=times,
-        maxvio=maxvio, e2e_ms=e2e_max, h2d=h2d, d2h=d2h, clocks=clocks, sweep=sweep,
+        maxvio=maxvio, e2e_ms=e2e_max, h2d=h2d, d2h=d2h, link_ms=link_ms, clocks=clocks, sweep=sweep,
         t_wall=(t_wall0, t_wall1), shape=s, HHp=HHp,
     )
     return res
@@ -708,6 +734,10 @@ def main():
         "e2e": {"value": round(whole_job_gbs(world, res["total_bytes"], res["e2e_ms"]), 1),
                 "unit": "GB/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
                 "ms_per_step": round(res["e2e_ms"], 4),
+                "copy_bound": {"ms_per_step": round(res["link_ms"], 4),
+                               "link_gbs": round((res["h2d"] + res["d2h"]) / res["link_ms"] / 1e6, 1),
+                               "frac": round(res["link_ms"] / res["e2e_ms"], 4),
+                               "note": "the same copies alone, both directions at once, no compute"},
                 "note": "every step: pinned host topk_idx/topk_w/hidden -> device, full step, "
                         "out+status -> host; copies on their own streams, double-buffered, overlapping "
                         "the neighbouring steps' compute; gradient tensors stay device-resident"},
