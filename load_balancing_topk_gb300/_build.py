@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libmep.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["abi.cu", "plan.cu", "permute.cu", "reduce_grad.cu", "prefetch.cu", "plan_static.cu",
-           "grouped_gemm.cu"]
+           "grouped_gemm.cu", "permute_backward.cu"]
 
 
 def nvcc() -> str:
