@@ -12,9 +12,12 @@
 //   k_hist     grid over tiles of <= 2048 assignments: per-tile expert counts
 //              (shared-memory atomics) and routing checks, one token per
 //              thread.
-//   k_plan     one CTA: tile counts -> T_e and per-group prefixes (16-byte
-//              column loads), home-first keep, overflow pour into deficits,
-//              slot table, cu_seqlens, per-expert row bases.
+//   k_gsum     (large tile tables only) one CTA per group of consecutive
+//              tiles: the group's per-expert sums, so that the planner reads
+//              Gs x E group sums instead of every tile's counts.
+//   k_plan     one CTA: tile (or group) counts -> T_e and per-group prefixes
+//              (16-byte column loads), home-first keep, overflow pour into
+//              deficits, slot table, cu_seqlens, per-expert row bases.
 //   k_offsets  grid over the same tiles: each assignment's index in its
 //              expert's token-ordered list (group prefix + earlier tiles of
 //              the group + warp prefix + rank inside the warp from
@@ -40,6 +43,9 @@ constexpr int kWarpIters = kTileAssign / (32 * kTileWarps);  // 8 iterations per
 constexpr int kPlanThreads = MEP_PLAN_THREADS;  // k_plan block size
 constexpr int kMaxScanGroups = 64;           // tile groups in k_plan's prefix pass
 constexpr int kPartInts = 8192;              // k_plan shared ints for group sums
+#ifndef MEP_PLAN_GSUM_MIN_INTS
+#define MEP_PLAN_GSUM_MIN_INTS 32768  // tile-count table size (ints) from which k_gsum runs
+#endif
 #ifndef MEP_PLAN_WARP_SCAN_MAX_E
 #define MEP_PLAN_WARP_SCAN_MAX_E 128
 #endif
@@ -50,7 +56,8 @@ inline int tile_tokens(int K) { return (kTileAssign / K) & ~3; }
 
 struct PlanWs {
   int* blockhist;    // [nblk, E] tile counts
-  int* groupbase;    // [E, Gs] count of e in all tiles before group g (Gs <= kMaxScanGroups)
+  int* groupbase;    // [Gs, E] count of e in all tiles before group g (Gs <= kMaxScanGroups)
+  int* groupsum;     // [Gs, E] count of e in group g (k_gsum; large tile tables only)
   int* blockerr;     // [nblk]
   int* keep;         // [E] tokens kept on the home row
   int* home_base;    // [E] global row of the home row's first token
@@ -72,6 +79,7 @@ size_t carve(PlanWs* ws, char* base, int nblk, int R, int E) {
   PlanWs* w = ws ? ws : &dummy;
   take(&w->blockhist, size_t(nblk) * E);
   take(&w->groupbase, size_t(kMaxScanGroups) * E);
+  take(&w->groupsum, size_t(kMaxScanGroups) * E);
   take(&w->blockerr, size_t(nblk > 0 ? nblk : 1));
   take(&w->keep, E);
   take(&w->home_base, E);
@@ -150,6 +158,7 @@ __global__ void __launch_bounds__(kTileThreads)
 struct PlanArgs {
   int nblk, R, S, K, E, B;
   int fallback;          // pieces beyond B take the expert's own row instead of failing
+  int presummed;         // k_gsum ran: read the group sums, not every tile's counts
   int32_t* counts;       // [E]
   int32_t* cu;           // [R, E+B]
   int32_t* slot_expert;  // [R, B]
@@ -211,42 +220,80 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT) {
   int Gs, tpg;
   tile_groups(nblk, E, &Gs, &tpg);
   const int P = part_pitch(Gs);
-  const V* h = reinterpret_cast<const V*>(a.ws.blockhist);
-  for (int x = tid; x < Gs * nc; x += nthr) {
-    const int g = x / nc, c = x - g * nc;
-    const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
+  if (a.presummed) {
+    // k_gsum already summed each group: Gs x E ints, one load each
+    const V* gsum = reinterpret_cast<const V*>(a.ws.groupsum);
+    for (int x = tid; x < Gs * nc; x += nthr) {
+      const int g = x / nc, c = x - g * nc;
+      const V v = __ldcg(gsum + x);
+#pragma unroll
+      for (int j = 0; j < W; ++j) sPart[(c * W + j) * P + g] = Vec<W>::get(v, j);
+    }
+  } else {
+    const V* h = reinterpret_cast<const V*>(a.ws.blockhist);
+    for (int x = tid; x < Gs * nc; x += nthr) {
+      const int g = x / nc, c = x - g * nc;
+      const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
+      int s[W];
+#pragma unroll
+      for (int j = 0; j < W; ++j) s[j] = 0;
+#pragma unroll 8
+      for (int b = b0; b < b1; ++b) {
+        const V v = h[size_t(b) * nc + c];
+#pragma unroll
+        for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
+      }
+#pragma unroll
+      for (int j = 0; j < W; ++j) sPart[(c * W + j) * P + g] = s[j];
+    }
+  }
+  __syncthreads();
+  // one thread per expert: exclusive scan over its Gs <= 64 group sums. The
+  // rows have odd pitch P, so a warp's 32 experts read 32 different banks;
+  // groupbase is group-major, so its writes (and k_offsets' reads) coalesce.
+  for (int e = tid; e < E; e += nthr) {
+    const int* row = sPart + e * P;
+    int run = 0;
+#pragma unroll 8
+    for (int g = 0; g < Gs; ++g) {
+      const int v = row[g];
+      a.ws.groupbase[g * E + e] = run;
+      run += v;
+    }
+    sT[e] = run;
+    a.counts[e] = run;
+  }
+  __syncthreads();
+}
+
+// k_gsum: CTA g sums the tile counts of its group of tpg consecutive tiles,
+// W experts per thread (all of a column's tile loads in flight together),
+// into groupsum[g][e].
+template <int W>
+__global__ void __launch_bounds__(kTileThreads)
+    k_gsum(const int* __restrict__ blockhist, int nblk, int E, int tpg, int* __restrict__ groupsum) {
+  pdl_wait();  // k_hist's counts
+  pdl_launch_dependents();
+  using V = typename Vec<W>::T;
+  const int nc = E / W, g = blockIdx.x;
+  const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
+  const V* h = reinterpret_cast<const V*>(blockhist);
+  V* out = reinterpret_cast<V*>(groupsum) + size_t(g) * nc;
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
     int s[W];
 #pragma unroll
     for (int j = 0; j < W; ++j) s[j] = 0;
 #pragma unroll 8
     for (int b = b0; b < b1; ++b) {
-      const V v = h[size_t(b) * nc + c];
+      const V v = __ldcg(h + size_t(b) * nc + c);
 #pragma unroll
       for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
     }
+    int t[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int j = 0; j < W; ++j) sPart[(c * W + j) * P + g] = s[j];
+    for (int j = 0; j < W; ++j) t[j] = s[j];
+    out[c] = Vec<W>::make(t);
   }
-  __syncthreads();
-  // one warp per expert: exclusive scan over its Gs <= 64 group sums (rows
-  // of odd pitch P: the column writes above hit 8 banks, the row reads
-  // below are conflict-free), written as groupbase[e][g]
-  const int lane = tid & 31;
-  for (int e = tid >> 5; e < E; e += nthr >> 5) {
-    const int* row = sPart + e * P;
-    const int v0 = lane < Gs ? row[lane] : 0;
-    const int v1 = lane + 32 < Gs ? row[lane + 32] : 0;
-    const int i0 = warp_incl_scan(v0);
-    const int tot0 = __shfl_sync(MEP_FULL_MASK, i0, 31);
-    const int i1 = warp_incl_scan(v1);
-    if (lane < Gs) a.ws.groupbase[e * Gs + lane] = i0 - v0;
-    if (lane + 32 < Gs) a.ws.groupbase[e * Gs + lane + 32] = tot0 + i1 - v1;
-    if (lane == 31) {
-      sT[e] = tot0 + i1;
-      a.counts[e] = tot0 + i1;
-    }
-  }
-  __syncthreads();
 }
 
 // Exclusive scan of a short array by warp 0 (out may alias in; out[n] =
@@ -557,7 +604,7 @@ __global__ void __launch_bounds__(kTileThreads)
   tile_groups(nblk, E, &Gs, &tpg);
   const int g = blk / tpg;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = __ldcg(ws.groupbase + e * Gs + g);
+    int run = __ldcg(ws.groupbase + size_t(g) * E + e);
     s_keep[e] = __ldcg(ws.keep + e);
     s_hb[e] = __ldcg(ws.home_base + e);
     s_pcb[e] = __ldcg(ws.pc_begin + e);
@@ -663,7 +710,22 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
     return MEP_ERR_CUDA;
 
   if (nblk > 0) k_hist<<<nblk, kTileThreads, hist_smem, st>>>(topk_idx, N, K, E, tpt, ws);
-  PlanArgs pa{nblk, R, S, K, E, B, fallback, expert_counts, cu_seqlens, slot_expert, status, ws};
+  // Beyond 128 KB of tile counts, the group sums are formed by Gs CTAs in
+  // parallel rather than inside the one planner CTA.
+  int Gs, tpg;
+  tile_groups(nblk, E, &Gs, &tpg);
+  const int presum = (long long)nblk * E >= MEP_PLAN_GSUM_MIN_INTS && Gs > 1 ? 1 : 0;
+  if (presum) {
+    const cudaError_t e =
+        (E & 3) == 0
+            ? launch_pdl(k_gsum<4>, dim3(Gs), dim3(kTileThreads), 0, st,
+                         static_cast<const int*>(ws.blockhist), nblk, E, tpg, ws.groupsum)
+            : launch_pdl(k_gsum<1>, dim3(Gs), dim3(kTileThreads), 0, st,
+                         static_cast<const int*>(ws.blockhist), nblk, E, tpg, ws.groupsum);
+    if (e != cudaSuccess) return MEP_ERR_CUDA;
+  }
+  PlanArgs pa{nblk,        R,         S,           K,      E, B, fallback, presum,
+              expert_counts, cu_seqlens, slot_expert, status, ws};
   if (launch_pdl(k_plan, dim3(1), dim3(kPlanThreads), plan_smem, st, pa) != cudaSuccess)
     return MEP_ERR_CUDA;
   if (nblk > 0 &&

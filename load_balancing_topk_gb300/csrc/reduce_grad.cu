@@ -23,7 +23,13 @@ namespace mep {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVecPerThread = 4;  // float4 vectors per thread per item
+#ifndef MEP_REDUCE_VEC
+#define MEP_REDUCE_VEC 4
+#endif
+#ifndef MEP_REDUCE_CTAS_PER_SM
+#define MEP_REDUCE_CTAS_PER_SM 2
+#endif
+constexpr int kVecPerThread = MEP_REDUCE_VEC;  // float4 vectors per thread per item
 #ifndef MEP_REDUCE_SLOT_BATCH
 #define MEP_REDUCE_SLOT_BATCH 4
 #endif
@@ -181,7 +187,7 @@ extern "C" int mep_reduce_grad(const int32_t* slot_expert, int E, int R, int B, 
   const void* fn = vec ? reinterpret_cast<const void*>(k_reduce_grad<true>)
                        : reinterpret_cast<const void*>(k_reduce_grad<false>);
   if (set_max_dynamic_smem(fn, smem)) return MEP_ERR_CUDA;
-  const int grid = sm_count() * 4;
+  const int grid = sm_count() * MEP_REDUCE_CTAS_PER_SM;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t err =
       vec ? launch_pdl(k_reduce_grad<true>, dim3(grid), dim3(kThreads), smem, st, slot_expert, E,
