@@ -6,9 +6,10 @@
 // 内存契约与权重布局 (E/R home rows per rank, B slot rows, cu_seqlens[E+B]).
 // maxvio and T_e: same page, section 解决的核心问题.
 //
-// Three launches, all asynchronous on the caller's stream; the second and
-// third use programmatic dependent launch, so each starts while its
-// predecessor drains and waits (griddepcontrol.wait) only before reading it:
+// Three launches (four for large tile tables), all asynchronous on the
+// caller's stream; all but the first use programmatic dependent launch, so
+// each starts while its predecessor drains and waits (griddepcontrol.wait)
+// only before reading it:
 //   k_hist     grid over tiles of <= 2048 assignments: per-tile expert counts
 //              (shared-memory atomics) and routing checks, one token per
 //              thread.
