@@ -105,6 +105,8 @@ def test_plan_random_small_sweep():
     (16, 4096, 1, 384, 24),   # K = 1: 4096-token tiles
     (2, 200, 64, 128, 4),     # K = 64 (the limit)
     (64, 64, 2, 512, 4),      # many ranks
+    (3, 20000, 5, 999, 64),   # group sums in their own kernel, one expert per thread (E % 4 != 0)
+    (8, 4000, 6, 400, 64),    # group sums in their own kernel, ragged last group of tiles
 ])
 def test_plan_edge_shapes(R, S, K, E, B):
     s = synth.Shape(R=R, E=E, K=K, S=S, H=8, B=B)
