@@ -45,6 +45,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "mep_common.cuh"
 
 #ifndef MEP_GEMM_B_LBO
@@ -767,18 +769,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once (thread-safe static init).
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -801,12 +802,17 @@ long long max_tiles(int R, int S, int K, int E, int B) {
   return ((long long)R * S * K + kBM - 1) / kBM + 2LL * R * (E + B);
 }
 
+// Per-device grid size of one GEMM kernel, found once (thread-safe).
+struct GridCache {
+  std::mutex mu;
+  int grid[64] = {};
+};
+
 // Launch a GEMM kernel as a persistent grid of clusters of CL CTAs: as many
 // clusters as can be resident at once (a cluster of 2 needs two free SMs of
-// one GPC), found once per device and kernel and cached by the caller.
+// one GPC), found once per device and kernel.
 template <typename Kernel>
-cudaError_t launch_gemm(Kernel kernel, int CL, int smem, int* cached_dev, int* cached_grid,
-                        cudaStream_t st,
+cudaError_t launch_gemm(Kernel kernel, int CL, int smem, GridCache& cache, cudaStream_t st,
                         const CUtensorMap& mx, const CUtensorMap& mh, const CUtensorMap& msl,
                         const int4* tiles, const int* count, int32_t* status, int E, int H,
                         int Hp, __nv_bfloat16* y, int st32) {
@@ -824,17 +830,21 @@ cudaError_t launch_gemm(Kernel kernel, int CL, int smem, int* cached_dev, int* c
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  if (dev != *cached_dev) {
-    int nclusters = 0;
-    cfg.gridDim = dim3(sm_count() / CL * CL);
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, kernel, &cfg);
-    if (e != cudaSuccess) return e;
-    if (nclusters < 1) return cudaErrorInvalidConfiguration;
-    *cached_grid = (nclusters * CL < sm_count() ? nclusters : sm_count() / CL) * CL;
-    *cached_dev = dev;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int grid = 0;
+  {
+    std::lock_guard<std::mutex> lock(cache.mu);
+    if (cache.grid[dev] == 0) {
+      int nclusters = 0;
+      cfg.gridDim = dim3(sm_count() / CL * CL);
+      const cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (nclusters < 1) return cudaErrorInvalidConfiguration;
+      cache.grid[dev] = (nclusters * CL < sm_count() ? nclusters : sm_count() / CL) * CL;
+    }
+    grid = cache.grid[dev];
   }
-  cfg.gridDim = dim3(*cached_grid);
+  cfg.gridDim = dim3(grid);
   return cudaLaunchKernelEx(&cfg, kernel, mx, mh, msl, tiles, count, status, E, H, Hp, y, st32);
 }
 
@@ -891,17 +901,17 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
   const int st32 =
       MEP_GEMM_ST32 && Hp % 16 == 0 && (reinterpret_cast<uintptr_t>(y) & 31u) == 0 ? 1 : 0;
   if (CL == 2 && MEP_GEMM_PAIR_MMA) {
-    static int dev_cache = -1, grid_cache = 0;
+    static GridCache cache;
     if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm_pair), kSmemPair))
       return MEP_ERR_CUDA;
-    err = launch_gemm(k_gemm_pair, 2, kSmemPair, &dev_cache, &grid_cache, st, mx, mh, msl, tiles,
-                      count, status, E, H, Hp, yb, st32);
+    err = launch_gemm(k_gemm_pair, 2, kSmemPair, cache, st, mx, mh, msl, tiles, count, status, E,
+                      H, Hp, yb, st32);
   } else {
-    static int dev_cache = -1, grid_cache = 0;
+    static GridCache cache;
     if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm<CL>), kSmemBytes))
       return MEP_ERR_CUDA;
-    err = launch_gemm(k_gemm<CL>, CL, kSmemBytes, &dev_cache, &grid_cache, st, mx, mh, msl,
-                      tiles, count, status, E, H, Hp, yb, st32);
+    err = launch_gemm(k_gemm<CL>, CL, kSmemBytes, cache, st, mx, mh, msl, tiles, count, status, E,
+                      H, Hp, yb, st32);
   }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
