@@ -328,6 +328,21 @@ MEP_API int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens, const
                              int B, int H, int Hp, void* ws, size_t ws_bytes, mep_bf16* y,
                              void* stream);
 
+/*
+ * mep_wait_selftest -- exercises the bounded wait that every pipeline wait
+ * of mep_grouped_gemm uses: one GPU thread waits on a barrier that nothing
+ * completes, with no copy or tensor-core operation in flight. After about
+ * limit_ns nanoseconds the wait gives up and writes MEP_ERR_TIMEOUT to
+ * *status (device int32; set only if it was 0); *elapsed_ns (device uint64)
+ * receives the nanoseconds it waited. For tests of the failure path: the GPU
+ * context stays usable.
+ *   limit_ns   0 .. 10^10
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG (null pointer, limit out of range),
+ * MEP_ERR_CUDA.
+ */
+MEP_API int mep_wait_selftest(int32_t* status, int64_t limit_ns, uint64_t* elapsed_ns,
+                              void* stream);
+
 #ifdef __cplusplus
 }
 #endif

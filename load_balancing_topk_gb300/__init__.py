@@ -72,6 +72,7 @@ SIGNATURES = [
     ("mep_grouped_gemm_workspace_bytes", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
     ("mep_grouped_gemm", _I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, ctypes.c_size_t,
                               _VP, _VP]),
+    ("mep_wait_selftest", _I, [_VP, ctypes.c_int64, _VP, _VP]),
 ]
 
 
@@ -424,3 +425,17 @@ def mep_grouped_gemm(x, cu_seqlens, w_home, w_slot, status, R: int, S: int, K: i
                                              _stream(dev))
     _check("mep_grouped_gemm", rc)
     return y
+
+
+def mep_wait_selftest(limit_ns: int, device=None):
+    """Run the bounded-wait self-test on the device; returns (status, elapsed_ns)
+    tensors (int32 [1], int64 [1]) after it is enqueued (not synchronised)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    elapsed = torch.zeros(1, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        rc = load_library().mep_wait_selftest(_ptr(status), int(limit_ns), _ptr(elapsed),
+                                              _stream(dev))
+    _check("mep_wait_selftest", rc)
+    return status, elapsed

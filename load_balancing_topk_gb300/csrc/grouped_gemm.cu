@@ -121,7 +121,8 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // at the end of the kernel pass honor_abort = false: they must see their own
 // copies and MMAs land before the CTA frees its TMEM and exits.
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort,
-                                             int32_t* status, bool honor_abort) {
+                                             int32_t* status, bool honor_abort,
+                                             uint64_t limit_ns = MEP_GEMM_TIMEOUT_NS) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -130,7 +131,7 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, vola
       const uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > MEP_GEMM_TIMEOUT_NS) {
+      } else if (now - t0 > limit_ns) {
         *abort = 1;
         set_status(status, MEP_ERR_TIMEOUT);
         return false;
@@ -763,6 +764,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives at, with no copy or MMA in flight. The wait must give up after
+// limit_ns and report MEP_ERR_TIMEOUT; *elapsed_ns gets the time it waited.
+__global__ void k_wait_selftest(int32_t* status, unsigned long long limit_ns,
+                                unsigned long long* elapsed_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const uint64_t t0 = globaltimer();
+  const bool ok = wait_phase_slow(smem_u32(&bar), 0u, &abort_flag, status, false, limit_ns);
+  *elapsed_ns = globaltimer() - t0;
+  if (ok) set_status(status, MEP_ERR_INVALID_ARG);  // cannot happen: nothing arrives
+}
+
+// ---------------------------------------------------------------------------
 // host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -914,4 +933,13 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
                       H, Hp, yb, st32);
   }
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
+}
+
+extern "C" int mep_wait_selftest(int32_t* status, int64_t limit_ns, uint64_t* elapsed_ns,
+                                 void* stream) {
+  if (status == nullptr || elapsed_ns == nullptr || limit_ns < 0 || limit_ns > 10000000000LL)
+    return MEP_ERR_INVALID_ARG;
+  k_wait_selftest<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      status, (unsigned long long)limit_ns, reinterpret_cast<unsigned long long*>(elapsed_ns));
+  return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }

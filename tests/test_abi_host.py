@@ -121,3 +121,12 @@ def test_prefetch_rejects_bad_args(lib):
     assert lib.mep_prefetch(None, 4, 2, 2, 64, 16, 16, None, None) == bad   # null map
     assert lib.mep_prefetch(16, 4, 2, 2, 64, 24, 16, None, None) == bad     # misaligned
     assert lib.mep_prefetch(None, 4, 2, 0, 64, None, None, None, None) == 0  # no slots
+
+
+def test_wait_selftest_rejects_bad_args(lib):
+    bad = mep.STATUS_CODE["MEP_ERR_INVALID_ARG"]
+    assert lib.mep_wait_selftest(None, 1000, 16, None) == bad          # null status
+    assert lib.mep_wait_selftest(16, 1000, None, None) == bad          # null elapsed
+    assert lib.mep_wait_selftest(16, -1, 16, None) == bad              # negative limit
+    assert lib.mep_wait_selftest(16, 10**10 + 1, 16, None) == bad      # limit beyond 10 s
+
