@@ -10,6 +10,8 @@
  *   mep_prefetch    redundant experts' weights copied into their slots
  *   mep_dispatch_backward / mep_combine_backward   the two permutes' gradients
  *   mep_grouped_gemm  the grouped expert product that consumes the buffer
+ *   mep_plan_remote_fallback / mep_plan_static_scratch   planner variants
+ *   mep_wait_selftest  the kernels' bounded wait, run on a barrier that never completes
  *
  * Sources (web pages about MoonEP, cited by title and section):
  *   "月之暗面开源MoonEP：面向MoE训练的专家并行通信库" -- sections
