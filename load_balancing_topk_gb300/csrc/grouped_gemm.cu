@@ -24,7 +24,8 @@
 //     warp 1      allocates the pair's TMEM (2 x 256 fp32 columns in each
 //                 CTA, cta_group::2) and, in CTA 0, issues from one lane the
 //                 pair MMAs (tcgen05.mma.cta_group::2: M = 256 over the two
-//                 CTAs, N = 256, K = 16, bf16 in, fp32 accumulate); every
+//                 CTAs, N = 256 -- 128 for a last column block of at most
+//                 128 columns --, K = 16, bf16 in, fp32 accumulate); every
 //                 commit is multicast to both CTAs (stage free, accumulator
 //                 ready);
 //     warps 2..5  epilogue of each CTA: tcgen05.ld of its 128 TMEM lanes
@@ -60,6 +61,9 @@
 #endif
 #ifndef MEP_GEMM_PAIR_MMA
 #define MEP_GEMM_PAIR_MMA 1  // clusters of 2 run k_gemm_pair (cta_group::2 MMAs)
+#endif
+#ifndef MEP_GEMM_NARROW_N
+#define MEP_GEMM_NARROW_N 1  // a last column block of <= 128 columns runs N = 128 pair MMAs
 #endif
 #ifndef MEP_GEMM_ST32
 #define MEP_GEMM_ST32 1  // epilogue stores whole 32-byte sectors when H' % 16 == 0
@@ -246,15 +250,19 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
 // The pair form: M = 256 rows over the two CTAs of a pair (each CTA's 128
 // rows of A and 128 of the 256 columns of B in its own shared memory, each
 // CTA's 128 rows of D in its own TMEM), issued by one thread of CTA 0.
+// kIdesc2n: the same with N = 128, for a last column block of at most 128
+// columns (each CTA then holds 64 of them).
 constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                              ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+constexpr uint32_t kIdesc2n = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                              ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
 __device__ __forceinline__ void tc_mma2(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t accumulate) {
+                                        uint32_t accumulate, uint32_t idesc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc2), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void tc_commit2_mc(uint32_t bar, uint16_t cta_mask) {
@@ -662,7 +670,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* wmap = home ? &map_wh : &map_ws;
         const int wrow = (home ? t.z : t.z - E) * H;
         const int left = (Hp - n0 + 63) / 64;
-        const int nbox = left < 4 ? left : 4;
+        const int nbox = left < 4 ? left : 4;  // 64-column boxes of the unit, both CTAs
+        // each CTA's share of the boxes: two (N = 256), or one when at most
+        // 128 columns remain and the MMAs run with N = 128
+        const bool narrow = MEP_GEMM_NARROW_N && Hp - n0 <= 128;
+        const int i0 = narrow ? rank : 2 * rank, i1 = narrow ? rank + 1 : 2 * rank + 2;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = int(it % kSt);
           const uint32_t round = it / kSt;
@@ -673,8 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb0 = map_to_rank(smem_u32(&S->full[s]), 0);
           if (leader) mbar_expect_tx(smem_u32(&S->full[s]), 2 * kABytes + nbox * kBBox);
           tma_load_2d_pair(sa + s * kABytes, &map_x, kb * kBK, t.x, fb0);
-          for (int i = 2 * rank; i < nbox && i < 2 * rank + 2; ++i)
-            tma_load_2d_pair(sb + s * kBHalf + (i - 2 * rank) * kBBox, wmap, n0 + 64 * i,
+          for (int i = i0; i < nbox && i < i1; ++i)
+            tma_load_2d_pair(sb + s * kBHalf + (i - i0) * kBBox, wmap, n0 + 64 * i,
                              wrow + kb * kBK, fb0);
           last_round[s] = int(round);
         }
@@ -701,6 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_phase(smem_u32(&S->tempty[a]), (use & 1u) ^ 1u, abort_flag, status)) break;
         tc_fence_after();
         const uint32_t d = tmem + a * kBN;
+        const int n0 = int(u % nN) * kBN;
+        const uint32_t idesc = MEP_GEMM_NARROW_N && Hp - n0 <= 128 ? kIdesc2n : kIdesc2;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = int(it % kSt);
           if (!wait_phase(smem_u32(&S->full[s]), (it / kSt) & 1u, abort_flag, status)) {
@@ -713,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ad = sdesc(sa + s * kABytes + kk * 32, 16, 1024);
             const uint64_t bd =
                 sdesc(sb + s * kBHalf + kk * 16 * 128, MEP_GEMM_B_LBO, MEP_GEMM_B_SBO);
-            tc_mma2(d, ad, bd, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma2(d, ad, bd, (kb | kk) != 0 ? 1u : 0u, idesc);
           }
           tc_commit2_mc(smem_u32(&S->empty[s]), 3);
         }
