@@ -631,6 +631,8 @@ def cpu_baseline(budget_s: float = 12.0) -> dict:
         r = dict(more, bytes=more["bytes"] + r["bytes"], seconds=more["seconds"] + r["seconds"],
                  reps=reps + 1)
     return {"value": round(r["bytes"] / r["seconds"] / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "host_cores": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+            else os.cpu_count(),
             "kind": "oracle",
             "sample": (f"{r['reps']} step(s) on {r['n_tok']} of 32768 tokens each (full plan; "
                        f"dispatch/combine of those tokens; reduce_grad on {frac:.3f} of each "
@@ -660,6 +662,8 @@ def reference_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(s, None),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "host_cores": len(os.sched_getaffinity(0))
+                             if hasattr(os, "sched_getaffinity") else os.cpu_count(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
