@@ -451,6 +451,16 @@ def next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp):
                                  "frac_of_peak": round(nb / ms / 1e6 / peak, 4),
                                  "slots": s.R * s.B, "bytes": nb}
     del home_w, slot_w
+    # reduce_grad with every slot in use (a seeded bijection onto experts
+    # homed elsewhere): 64 slots onto 64 experts, fp32 E64 x 2048 x 1408
+    home_g = torch.randn((s.E, HHp), generator=g, device=dev) * 1e-3
+    slot_g = torch.randn((s.R * s.B, HHp), generator=g, device=dev) * 1e-3
+    ms = timed(lambda: mep.mep_reduce_grad(full, home_g, slot_g, None, s.E))
+    nb = 2 * (s.R * s.B + s.E) * HHp * 4
+    res["reduce_grad_all_slots"] = {"ms": round(ms, 4), "gbs": round(nb / ms / 1e6, 1),
+                                    "frac_of_peak": round(nb / ms / 1e6 / peak, 4),
+                                    "slots": s.R * s.B, "experts": s.E, "bytes": nb}
+    del home_g, slot_g
     dh = torch.empty((s.N, s.H), dtype=torch.bfloat16, device=dev)
     ms = timed(lambda: mep.mep_dispatch_backward(buf, plan.dst_pos, plan.status, s.R, s.S, s.K,
                                                  dhidden=dh))
