@@ -213,14 +213,18 @@ __host__ __device__ inline void tile_groups(int nblk, int E, int* Gs, int* tpg) 
   *tpg = nblk > 0 ? (nblk + g - 1) / g : 1;
 }
 
+// Also collects k_hist's error words: their loads go out with the counts,
+// and the lowest failing tile lands in *s_errblk (initialised before the
+// call) by the end.
 template <int W>
-__device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT) {
+__device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT, int* s_errblk) {
   using V = typename Vec<W>::T;
   const int E = a.E, nblk = a.nblk, nthr = blockDim.x, tid = threadIdx.x;
   const int nc = E / W;
   int Gs, tpg;
   tile_groups(nblk, E, &Gs, &tpg);
   const int P = part_pitch(Gs);
+  const int err0 = tid < nblk ? __ldcg(a.ws.blockerr + tid) : 0;  // in flight with the counts
   if (a.presummed) {
     // k_gsum already summed each group: Gs x E ints, one load each
     const V* gsum = reinterpret_cast<const V*>(a.ws.groupsum);
@@ -249,9 +253,17 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT) {
     }
   }
   __syncthreads();
+  {
+    int bad = err0 != 0 ? tid : INT_MAX;
+    for (int b = tid + nthr; b < nblk; b += nthr)
+      if (bad == INT_MAX && __ldcg(a.ws.blockerr + b) != 0) bad = b;
+    if (bad != INT_MAX) atomicMin(s_errblk, bad);
+  }
   // one thread per expert: exclusive scan over its Gs <= 64 group sums. The
   // rows have odd pitch P, so a warp's 32 experts read 32 different banks;
-  // groupbase is group-major, so its writes (and k_offsets' reads) coalesce.
+  // groupbase is group-major, so a warp's writes of one group coalesce (and
+  // so do k_offsets' reads). (Splitting an expert's groups over several
+  // lanes measured slower: its group-major writes no longer coalesce.)
   for (int e = tid; e < E; e += nthr) {
     const int* row = sPart + e * P;
     int run = 0;
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   pdl_wait();                // k_hist's counts and error words
   pdl_launch_dependents();
   extern __shared__ int smem[];
-  const int E = a.E, R = a.R, B = a.B, nblk = a.nblk;
+  const int E = a.E, R = a.R, B = a.B;
   const int per = E / R;
   const int SK = a.S * a.K;
   const int G = E + B;
@@ -346,23 +358,18 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   __shared__ int s_warp[33];
   __shared__ int s_errblk, s_cap;
 
-  // 0. routing errors found by k_hist (lowest tile wins)
-  if (tid == 0) {
+  if (tid == 0) {  // ordered before every use by the barriers in tile_group_sums
     s_errblk = INT_MAX;
     s_cap = 0;
   }
-  __syncthreads();
-  for (int b = tid; b < nblk; b += nthr)
-    if (a.ws.blockerr[b] != 0) atomicMin(&s_errblk, b);
-  __syncthreads();
+  // 1. T_e and the per-group prefixes of the tile counts; with them, the
+  //    routing errors k_hist found (lowest tile wins)
+  if ((E & 3) == 0) tile_group_sums<4>(a, sPart, sT, &s_errblk);
+  else tile_group_sums<1>(a, sPart, sT, &s_errblk);
   if (s_errblk != INT_MAX) {
     plan_fail(a, a.ws.blockerr[s_errblk], true);
     return;
   }
-
-  // 1. T_e and the per-group prefixes of the tile counts
-  if ((E & 3) == 0) tile_group_sums<4>(a, sPart, sT);
-  else tile_group_sums<1>(a, sPart, sT);
 
   // 2. home-first keep: the count of e's earlier home experts is a
   //    difference of the running sum of T; then
@@ -402,6 +409,20 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
         sOst[E] = cO;
         sFlag[E] = cF;
       }
+      __syncwarp();
+      // deficits S*K - load_r (rank order) and their exclusive running sum
+      int cD = 0;
+      for (int r0 = 0; r0 < R; r0 += 32) {
+        const int r = r0 + lane;
+        const int d = r < R ? max(0, SK - (sPre[(r + 1) * per] - sPre[r * per])) : 0;
+        const int iD = warp_incl_scan(d);
+        if (r < R) {
+          sDef[r] = d;
+          sDst[r] = cD + iD - d;
+        }
+        cD += __shfl_sync(MEP_FULL_MASK, iD, 31);
+      }
+      if (lane == 0) sDst[R] = cD;
     }
     __syncthreads();
   } else {
@@ -420,17 +441,21 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     block_excl_scan(sFlag, sFlag, E, s_warp, true);
     for (int e = tid; e < E; e += nthr)
       if (sOv[e] > 0) sOlist[sFlag[e]] = e;
+    for (int r = tid; r < R; r += nthr)
+      sDef[r] = max(0, SK - (sPre[(r + 1) * per] - sPre[r * per]));
+    __syncthreads();
+    warp0_excl_scan(sDef, sDst, R);
   }
-  for (int r = tid; r < R; r += nthr)
-    sDef[r] = max(0, SK - (sPre[(r + 1) * per] - sPre[r * per]));
-  __syncthreads();
-  warp0_excl_scan(sDef, sDst, R);
   const int nov = sFlag[E];
 
   // 4. pieces of each under-loaded rank: the overflow segments that meet
   //    [Dst_r, Dst_r + d_r), in expert order, one slot each. First count
   //    them (and find the first segment), then number them globally in rank
   //    order, then write them.
+  for (int e = tid; e < E; e += nthr) {  // per-expert piece tables, filled below
+    sPcBeg[e] = INT_MAX;
+    sPcCnt[e] = 0;
+  }
   for (int r = tid; r < R; r += nthr) {
     int np = 0, q0 = 0;
     const int d = sDef[r];
@@ -460,11 +485,6 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     return;
   }
   warp0_excl_scan(sNp, sPex, R);
-  for (int e = tid; e < E; e += nthr) {
-    sPcBeg[e] = INT_MAX;
-    sPcCnt[e] = 0;
-  }
-  __syncthreads();
   for (int r = tid; r < R; r += nthr) {
     const int np = sNp[r];
     const int lo = sDst[r], hi = lo + sDef[r];
@@ -488,43 +508,51 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     a.ws.pc_count[e] = sPcCnt[e];
   }
 
-  // 5. cu_seqlens, one warp per rank; also the global first row of every
-  //    home row and piece.
-  //    Pieces b < B sit in slot rows E + b; pieces b >= B (fallback only)
-  //    sit in the expert's own row e, found by a binary search over the
-  //    rank's remaining pieces, whose experts ascend with b.
+  // 5. cu_seqlens; also the global first row of every home row and piece.
+  //    Row j of rank r: home rows keep their kept count, slot rows E + b
+  //    hold piece b < B, and pieces b >= B (fallback only) sit in the
+  //    expert's own row e, found by a binary search over the rank's
+  //    remaining pieces, whose experts ascend with b. g = the piece, or -1.
+  auto row_count = [&](int r, int j, int& g) -> int {
+    g = -1;
+    const int np = sNp[r];
+    if (j < E) {
+      if (j / per == r) return sKeep[j];
+      if (np > B) {
+        const int q0 = sQ0[r];
+        int lo = B, hi = np;
+        while (lo < hi) {
+          const int m = (lo + hi) >> 1;
+          if (sOlist[q0 + m] < j) lo = m + 1; else hi = m;
+        }
+        if (lo < np && sOlist[q0 + lo] == j) {
+          g = sPex[r] + lo;
+          return sPlen[g];
+        }
+      }
+      return 0;
+    }
+    if (j < G && j - E < min(np, B)) {
+      g = sPex[r] + (j - E);
+      return sPlen[g];
+    }
+    return 0;
+  };
+  auto write_row = [&](int r, int j, int c, int g, int incl_end) {
+    a.cu[size_t(r) * G + j] = incl_end;
+    const int start = r * SK + incl_end - c;
+    if (j < E && j / per == r) a.ws.home_base[j] = start;
+    else if (g >= 0) a.ws.piece_base[g] = start;
+  };
+  // one warp per rank, its chunks of 32 rows in order
   for (int r = warp; r < R; r += nwarps) {
     int carry = 0;
-    const int np = sNp[r], pex = sPex[r], q0 = sQ0[r];
-    const int nslot = min(np, B);
     for (int j0 = 0; j0 < G; j0 += 32) {
       const int j = j0 + lane;
-      int c = 0, g = -1;
-      if (j < E) {
-        if (j / per == r) {
-          c = sKeep[j];
-        } else if (np > B) {
-          int lo = B, hi = np;
-          while (lo < hi) {
-            const int m = (lo + hi) >> 1;
-            if (sOlist[q0 + m] < j) lo = m + 1; else hi = m;
-          }
-          if (lo < np && sOlist[q0 + lo] == j) {
-            g = pex + lo;
-            c = sPlen[g];
-          }
-        }
-      } else if (j < G && j - E < nslot) {
-        g = pex + (j - E);
-        c = sPlen[g];
-      }
+      int g;
+      const int c = j < G ? row_count(r, j, g) : 0;
       const int incl = warp_incl_scan(c);
-      if (j < G) {
-        a.cu[size_t(r) * G + j] = carry + incl;
-        const int start = r * SK + carry + incl - c;
-        if (j < E && j / per == r) a.ws.home_base[j] = start;
-        else if (g >= 0) a.ws.piece_base[g] = start;
-      }
+      if (j < G) write_row(r, j, c, g, carry + incl);
       carry += __shfl_sync(MEP_FULL_MASK, incl, 31);
     }
   }
