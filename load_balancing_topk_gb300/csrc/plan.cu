@@ -309,6 +309,56 @@ __global__ void __launch_bounds__(kTileThreads)
   }
 }
 
+// Three exclusive block scans in one pass (out_i may alias in_i; out_i[n]
+// gets the total): one round of warp scans and one pair of barriers for all
+// three. s_w holds >= 3 * 33 ints. Ends with __syncthreads().
+__device__ void block_excl_scan3(const int* in0, int* out0, const int* in1, int* out1,
+                                 const int* in2, int* out2, int n, int* s_w) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = (nthr + 31) >> 5;
+  const int per = (n + nthr - 1) / nthr;
+  const int beg = min(n, tid * per), end = min(n, beg + per);
+  int l0 = 0, l1 = 0, l2 = 0;
+  for (int i = beg; i < end; ++i) {
+    l0 += in0[i];
+    l1 += in1[i];
+    l2 += in2[i];
+  }
+  const int i0 = warp_incl_scan(l0), i1 = warp_incl_scan(l1), i2 = warp_incl_scan(l2);
+  if (lane == 31) {
+    s_w[warp] = i0;
+    s_w[33 + warp] = i1;
+    s_w[66 + warp] = i2;
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int v = lane < nwarps ? s_w[33 * q + lane] : 0;
+      const int vi = warp_incl_scan(v);
+      s_w[33 * q + lane] = vi - v;
+      if (lane == 31) s_w[33 * q + 32] = vi;
+    }
+  }
+  __syncthreads();
+  int r0 = s_w[warp] + i0 - l0, r1 = s_w[33 + warp] + i1 - l1, r2 = s_w[66 + warp] + i2 - l2;
+  for (int i = beg; i < end; ++i) {
+    const int v0 = in0[i], v1 = in1[i], v2 = in2[i];
+    out0[i] = r0;
+    out1[i] = r1;
+    out2[i] = r2;
+    r0 += v0;
+    r1 += v1;
+    r2 += v2;
+  }
+  if (tid == 0) {
+    out0[n] = s_w[32];
+    out1[n] = s_w[65];
+    out2[n] = s_w[98];
+  }
+  __syncthreads();
+}
+
 // Exclusive scan of a short array by warp 0 (out may alias in; out[n] =
 // total). Ends with __syncthreads().
 __device__ void warp0_excl_scan(const int* in, int* out, int n) {
@@ -355,12 +405,13 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   int* sNp = sDst + RP;          // [R+1]
   int* sPex = sNp + RP;          // [R+1]
   int* sQ0 = sPex + RP;          // [R+1] first overflow segment of each rank
-  __shared__ int s_warp[33];
-  __shared__ int s_errblk, s_cap;
+  __shared__ int s_warp[3 * 33];
+  __shared__ int s_errblk, s_cap, s_over;
 
   if (tid == 0) {  // ordered before every use by the barriers in tile_group_sums
     s_errblk = INT_MAX;
     s_cap = 0;
+    s_over = 0;
   }
   // 1. T_e and the per-group prefixes of the tile counts; with them, the
   //    routing errors k_hist found (lowest tile wins)
@@ -377,9 +428,11 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   //    line. Up to 128 experts, warp 0 does both in one pass over chunks
   //    of 32 experts (three warp scans per chunk, no block barrier);
   //    beyond, block-wide scans (faster on GB300 from E = 256 on).
+  // (the group sums are consumed: sPart now holds the running sum of keep)
+  int* sKpre = sPart;  // [E+1] exclusive prefix of keep, total at E
   if (E <= MEP_PLAN_WARP_SCAN_MAX_E) {
     if (warp == 0) {
-      int cT = 0, cO = 0, cF = 0;
+      int cT = 0, cO = 0, cF = 0, cK = 0;
       for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
         const int T = e < E ? sT[e] : 0;
@@ -399,6 +452,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
         const int iO = warp_incl_scan(ov);
         if (e < E) sOst[e] = cO + iO - ov;
         cO += __shfl_sync(MEP_FULL_MASK, iO, 31);
+        const int kp = e < E ? T - ov : 0;
+        const int iK = warp_incl_scan(kp);
+        if (e < E) sKpre[e] = cK + iK - kp;
+        cK += __shfl_sync(MEP_FULL_MASK, iK, 31);
         const int f = ov > 0 ? 1 : 0;
         const int iF = warp_incl_scan(f);
         if (f) sOlist[cF + iF - 1] = e;
@@ -408,6 +465,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
         sPre[E] = cT;
         sOst[E] = cO;
         sFlag[E] = cF;
+        sKpre[E] = cK;
       }
       __syncwarp();
       // deficits S*K - load_r (rank order) and their exclusive running sum
@@ -437,8 +495,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
       a.ws.keep[e] = kp;
     }
     __syncthreads();
-    block_excl_scan(sOv, sOst, E, s_warp, true);
-    block_excl_scan(sFlag, sFlag, E, s_warp, true);
+    block_excl_scan3(sOv, sOst, sFlag, sFlag, sKeep, sKpre, E, s_warp);
     for (int e = tid; e < E; e += nthr)
       if (sOv[e] > 0) sOlist[sFlag[e]] = e;
     for (int r = tid; r < R; r += nthr)
@@ -475,7 +532,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
         if (min(oe, hi) < oe) break;
       }
     }
-    if (np > B && !a.fallback) s_cap = 1;
+    if (np > B) {
+      if (!a.fallback) s_cap = 1;
+      s_over = 1;  // inference: pieces beyond B sit in home rows
+    }
     sNp[r] = np;
     sQ0[r] = q0;
   }
@@ -544,7 +604,34 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     if (j < E && j / per == r) a.ws.home_base[j] = start;
     else if (g >= 0) a.ws.piece_base[g] = start;
   };
-  // one warp per rank, its chunks of 32 rows in order
+  if (!s_over) {
+    // Every piece sits in a slot row (no inference overflow), so every entry
+    // has a closed form and all R x (E+B) are written in one parallel pass.
+    // Rank r keeps SK - d_r tokens on its home rows (their running sum is a
+    // difference of the keep prefix); slot piece b covers [max(os, lo),
+    // min(oe, lo + d_r)) of the overflow line, lo the rank's start on it, so
+    // it starts at SK - d_r + (max(os, lo) - lo) in the rank's buffer.
+    for (int i = tid; i < R * G; i += nthr) {
+      const int r = i / G, j = i - r * G;
+      const int s0 = r * per, d = sDef[r];
+      int c;
+      if (j < E) {
+        c = j < s0 ? 0 : sKpre[min(j + 1, s0 + per)] - sKpre[s0];
+        if (j >= s0 && j < s0 + per) a.ws.home_base[j] = r * SK + sKpre[j] - sKpre[s0];
+      } else if (j - E < sNp[r]) {
+        const int b = j - E, e = sOlist[sQ0[r] + b];
+        const int lo = sDst[r], os = sOst[e], oe = os + sOv[e];
+        c = SK - d + (min(oe, lo + d) - lo);
+        a.ws.piece_base[sPex[r] + b] = r * SK + SK - d + (max(os, lo) - lo);
+      } else {
+        c = SK;
+      }
+      a.cu[size_t(r) * G + j] = c;
+    }
+    if (tid == 0) *a.status = MEP_OK;
+    return;
+  }
+  // inference overflow present: one warp per rank, its chunks of 32 rows in order
   for (int r = warp; r < R; r += nwarps) {
     int carry = 0;
     for (int j0 = 0; j0 < G; j0 += 32) {
