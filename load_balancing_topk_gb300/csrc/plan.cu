@@ -18,7 +18,8 @@
 //              Gs x E group sums instead of every tile's counts.
 //   k_plan     one CTA: tile (or group) counts -> T_e and per-group prefixes
 //              (16-byte column loads), home-first keep, overflow pour into
-//              deficits, slot table, cu_seqlens, per-expert row bases.
+//              deficits, slot table, then cu_seqlens and the row bases in
+//              closed form (one parallel pass).
 //   k_offsets  grid over the same tiles: each assignment's index in its
 //              expert's token-ordered list (group prefix + earlier tiles of
 //              the group + warp prefix + rank inside the warp from
