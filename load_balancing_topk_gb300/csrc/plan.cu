@@ -668,8 +668,8 @@ __global__ void __launch_bounds__(kTileThreads)
   const int ntok = min(tok_per_tile, N - t0);
   const int na = ntok * K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // Everything up to the wait depends only on this tile's routing, so it
-  // overlaps the planner: stage the tile, then rank each assignment among
+  // Everything up to the wait depends only on the routing and on k_hist, so
+  // it overlaps the planner: stage the tile, then rank each assignment among
   // the tile's assignments of the same expert.
   {
     const int32_t* g = topk_idx + size_t(t0) * K;
@@ -712,21 +712,16 @@ __global__ void __launch_bounds__(kTileThreads)
   }
   __syncthreads();
 
-  pdl_wait();                           // the planner's tables and status
-  pdl_launch_dependents();
-  const int st = status != nullptr ? __ldcg(status) : 0;
-  // per expert: the tile's prefix (the group's base plus the group's earlier
-  // tiles) and the planner's tables, all loads issued together
+  // The tile's offsets from its group's base need no wait either: the
+  // group's earlier tiles come from k_hist, which has completed before this
+  // grid can start (the planner releases it only after its own wait on
+  // k_hist). Then each assignment's expert and offset go to registers.
   int Gs, tpg;
   tile_groups(nblk, E, &Gs, &tpg);
   const int g = blk / tpg;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = __ldcg(ws.groupbase + size_t(g) * E + e);
-    s_keep[e] = __ldcg(ws.keep + e);
-    s_hb[e] = __ldcg(ws.home_base + e);
-    s_pcb[e] = __ldcg(ws.pc_begin + e);
-    s_pcn[e] = __ldcg(ws.pc_count + e);
-#pragma unroll 4
+    int run = 0;
+#pragma unroll 8
     for (int b = g * tpg; b < blk; ++b) run += __ldcg(ws.blockhist + size_t(b) * E + e);
 #pragma unroll
     for (int w = 0; w < kTileWarps; ++w) {
@@ -734,6 +729,29 @@ __global__ void __launch_bounds__(kTileThreads)
       s_wcnt[w * E + e] = run;
       run += v;
     }
+  }
+  __syncthreads();
+  int ej[kWarpIters], rel[kWarpIters];
+#pragma unroll
+  for (int j = 0; j < kWarpIters; ++j) {
+    const int a = wbeg + j * 32 + lane;
+    const int e = a < wend ? s_idx[a] : -1;
+    const bool in = e >= 0 && e < E;  // bad ids: the planner's status stops us below
+    ej[j] = in ? e : 0;
+    rel[j] = in ? wc[e] + loc[j] : 0;
+  }
+  __syncthreads();  // s_wcnt is reused below
+
+  pdl_wait();                           // the planner's tables and status
+  pdl_launch_dependents();
+  const int st = status != nullptr ? __ldcg(status) : 0;
+  int* s_gb = s_wcnt;                   // [E] the group's base, per expert
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    s_gb[e] = __ldcg(ws.groupbase + size_t(g) * E + e);
+    s_keep[e] = __ldcg(ws.keep + e);
+    s_hb[e] = __ldcg(ws.home_base + e);
+    s_pcb[e] = __ldcg(ws.pc_begin + e);
+    s_pcn[e] = __ldcg(ws.pc_count + e);
   }
   if (pieces_smem)
     for (int q = threadIdx.x; q < E + R; q += blockDim.x) {
@@ -747,8 +765,8 @@ __global__ void __launch_bounds__(kTileThreads)
   for (int j = 0; j < kWarpIters; ++j) {
     const int a = wbeg + j * 32 + lane;
     if (a < wend) {
-      const int e = s_idx[a];
-      const int i = wc[e] + loc[j];     // index of the token in expert e's list
+      const int e = ej[j];
+      const int i = s_gb[e] + rel[j];   // index of the token in expert e's list
       int row;
       if (i < s_keep[e]) {
         row = s_hb[e] + i;
