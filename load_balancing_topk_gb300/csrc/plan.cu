@@ -545,23 +545,31 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     plan_fail(a, MEP_ERR_CAPACITY, false);
     return;
   }
-  warp0_excl_scan(sNp, sPex, R);
-  for (int r = tid; r < R; r += nthr) {
-    const int np = sNp[r];
-    const int lo = sDst[r], hi = lo + sDef[r];
-    for (int b = 0; b < np; ++b) {
-      const int e = sOlist[sQ0[r] + b];
-      const int os = sOst[e], oe = os + sOv[e];
-      const int s = max(os, lo), en = min(oe, hi);
-      const int g = sPex[r] + b;
-      if (g >= E + R) break;  // cannot happen: pieces <= overflow experts + deficit ranks - 1
-      if (b < B) a.slot_expert[r * B + b] = e;
-      a.ws.piece_lo[g] = sKeep[e] + (s - os);
-      sPlen[g] = en - s;
-      atomicMin(&sPcBeg[e], g);
-      atomicAdd(&sPcCnt[e], 1);
+  warp0_excl_scan(sNp, sPex, R);  // sPex[R]: pieces in all
+  // slot table, one thread per (rank, slot): the rank's b-th piece's expert,
+  // or -1 (pieces beyond B, inference only, have no slot)
+  for (int i = tid; i < R * B; i += nthr) {
+    const int r = i / B, b = i - r * B;
+    a.slot_expert[i] = b < sNp[r] ? sOlist[sQ0[r] + b] : -1;
+  }
+  // pieces, one thread each; its rank is the last r with sPex[r] <= g
+  // (empty ranks repeat their successor's start, so the last one is right)
+  const int npieces = min(sPex[R], E + R);  // <= overflow experts + deficit ranks - 1
+  for (int g = tid; g < npieces; g += nthr) {
+    int lo = 0, hi = R;
+    while (hi - lo > 1) {
+      const int m = (lo + hi) >> 1;
+      if (sPex[m] <= g) lo = m; else hi = m;
     }
-    for (int b = np; b < B; ++b) a.slot_expert[r * B + b] = -1;
+    const int r = lo, b = g - sPex[r];
+    const int e = sOlist[sQ0[r] + b];
+    const int os = sOst[e], oe = os + sOv[e];
+    const int dlo = sDst[r], dhi = dlo + sDef[r];
+    const int st = max(os, dlo), en = min(oe, dhi);
+    a.ws.piece_lo[g] = sKeep[e] + (st - os);
+    sPlen[g] = en - st;
+    atomicMin(&sPcBeg[e], g);
+    atomicAdd(&sPcCnt[e], 1);
   }
   __syncthreads();
   for (int e = tid; e < E; e += nthr) {
