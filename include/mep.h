@@ -285,12 +285,15 @@ MEP_API int mep_combine_backward(const mep_bf16* dout, const mep_bf16* y, const 
  *   slot_expert int32 [R, B]          from mep_plan (or any map into [-1, E))
  *   E, R, B                           sizes
  *   HHp         int64                 elements per expert matrix (H * H')
- *   home_grad   fp32 [E, HHp]         in/out
- *   slot_grad   fp32 [R, B, HHp]      in/out; must not overlap home_grad
+ *   home_grad   fp32 [E, HHp]         in/out, 16-byte aligned
+ *   slot_grad   fp32 [R, B, HHp]      in/out, 16-byte aligned; must not overlap
+ *                                     home_grad (32-byte alignment of both and
+ *                                     HHp % 8 == 0 select 32-byte accesses)
  *   status      int32 [1]             read on entry (nonzero: no-op); set to
  *                                     MEP_ERR_BAD_SLOT_MAP (nothing changed)
  *                                     if an entry is outside [-1, E). May be NULL.
- * Host returns: MEP_OK, MEP_ERR_INVALID_ARG, MEP_ERR_CUDA.
+ * Host returns: MEP_OK, MEP_ERR_INVALID_ARG (also for a misaligned buffer),
+ * MEP_ERR_CUDA.
  */
 MEP_API int mep_reduce_grad(const int32_t* slot_expert, int E, int R, int B, int64_t HHp,
                     float* home_grad, float* slot_grad, int32_t* status, void* stream);

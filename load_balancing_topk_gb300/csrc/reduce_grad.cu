@@ -13,9 +13,11 @@
 // expert, the list of its slots in (r, b) order (warp-aggregated stable
 // counting in shared memory), and the list of experts that have slots. The
 // work is then (used expert, element chunk) items, walked grid-stride: each
-// thread loads the home vector and all of the expert's slot vectors (16-byte
-// float4, all in flight together), adds them in (r, b) order in fp32, writes
-// the home vector and writes zeros over the consumed slot vectors.
+// thread loads the home vector and all of the expert's slot vectors (all in
+// flight together), adds them in (r, b) order in fp32, writes the home
+// vector and writes zeros over the consumed slot vectors. Vectors are
+// 32 bytes (8 floats, ld/st .v8) when H*H' % 8 == 0 and both buffers are
+// 32-byte aligned, else 16 bytes, else single floats.
 
 #include "mep_common.cuh"
 
@@ -23,26 +25,91 @@ namespace mep {
 namespace {
 
 constexpr int kThreads = 256;
-#ifndef MEP_REDUCE_VEC
-#define MEP_REDUCE_VEC 4
-#endif
 #ifndef MEP_REDUCE_CTAS_PER_SM
 #define MEP_REDUCE_CTAS_PER_SM 2
 #endif
-constexpr int kVecPerThread = MEP_REDUCE_VEC;  // float4 vectors per thread per item
+#ifndef MEP_REDUCE_V32
+#define MEP_REDUCE_V32 1  // 32-byte accesses when the sizes and addresses allow
+#endif
+#ifndef MEP_REDUCE_THREAD_BYTES
+#define MEP_REDUCE_THREAD_BYTES 64  // bytes of each matrix a thread moves per item
+#endif
 #ifndef MEP_REDUCE_SLOT_BATCH
 #define MEP_REDUCE_SLOT_BATCH 4
 #endif
 constexpr int kSlotBatch = MEP_REDUCE_SLOT_BATCH;  // slot vectors loaded together
-
-__device__ __forceinline__ void add4(float4& a, const float4& b) {
-  a.x = __fadd_rn(a.x, b.x);
-  a.y = __fadd_rn(a.y, b.y);
-  a.z = __fadd_rn(a.z, b.z);
-  a.w = __fadd_rn(a.w, b.w);
+// vectors of W floats per thread per item
+template <int W> __host__ __device__ constexpr int vec_per_thread() {
+  return MEP_REDUCE_THREAD_BYTES / (4 * W) > 0 ? MEP_REDUCE_THREAD_BYTES / (4 * W) : 1;
 }
 
-template <bool VEC>
+// W consecutive fp32 values moved as one access: 1 (scalar), 4 (16 bytes) or
+// 8 (32 bytes, ld/st .v8, sm_100 and later). Every access is volatile asm or
+// volatile-equivalent so that a slot load is never moved past the store of
+// zeros to the same address. Home loads and stores use the default caching;
+// slot loads and the zero stores stream (.cs): nothing reads them again.
+template <int W> struct Vec;
+template <> struct Vec<1> {
+  float v[1];
+  static __device__ __forceinline__ Vec ld(const float* p) { return Vec{{*p}}; }
+  static __device__ __forceinline__ Vec ld_cs(const float* p) { return Vec{{__ldcs(p)}}; }
+  __device__ __forceinline__ void st(float* p) const { *p = v[0]; }
+  static __device__ __forceinline__ void st_zero_cs(float* p) { __stcs(p, 0.f); }
+};
+template <> struct Vec<4> {
+  float v[4];
+  static __device__ __forceinline__ Vec from(const float4& q) { return Vec{{q.x, q.y, q.z, q.w}}; }
+  static __device__ __forceinline__ Vec ld(const float* p) {
+    return from(*reinterpret_cast<const float4*>(p));
+  }
+  static __device__ __forceinline__ Vec ld_cs(const float* p) {
+    return from(__ldcs(reinterpret_cast<const float4*>(p)));
+  }
+  __device__ __forceinline__ void st(float* p) const {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  static __device__ __forceinline__ void st_zero_cs(float* p) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(0.f, 0.f, 0.f, 0.f));
+  }
+};
+template <> struct Vec<8> {
+  float v[8];
+  static __device__ __forceinline__ Vec ld(const float* p) {
+    Vec r;
+    asm volatile("ld.global.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]),
+                   "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
+                 : "l"(p)
+                 : "memory");
+    return r;
+  }
+  static __device__ __forceinline__ Vec ld_cs(const float* p) {
+    Vec r;
+    asm volatile("ld.global.cs.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]),
+                   "=f"(r.v[5]), "=f"(r.v[6]), "=f"(r.v[7])
+                 : "l"(p)
+                 : "memory");
+    return r;
+  }
+  __device__ __forceinline__ void st(float* p) const {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]),
+                 "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+  }
+  static __device__ __forceinline__ void st_zero_cs(float* p) {
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1};" ::"l"(p), "f"(0.f)
+                 : "memory");
+  }
+};
+
+template <int W>
+__device__ __forceinline__ void add_rn(Vec<W>& a, const Vec<W>& b) {
+#pragma unroll
+  for (int j = 0; j < W; ++j) a.v[j] = __fadd_rn(a.v[j], b.v[j]);
+}
+
+template <int W>
 __global__ void __launch_bounds__(kThreads)
     k_reduce_grad(const int32_t* __restrict__ slot_expert, int E, int RB, long long HHp,
                   float* __restrict__ home, float* __restrict__ slot, int32_t* status) {
@@ -102,7 +169,8 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   const int nused = s_fill[E];
 
-  const long long nvec = VEC ? HHp / 4 : HHp;  // vectors (or scalars) per matrix
+  constexpr int kVecPerThread = vec_per_thread<W>();
+  const long long nvec = HHp / W;  // vectors per matrix (the host checks HHp % W == 0)
   const long long per_item = (long long)kThreads * kVecPerThread;
   const long long nchunk = (nvec + per_item - 1) / per_item;
   const long long items = (long long)nused * nchunk;
@@ -112,58 +180,44 @@ __global__ void __launch_bounds__(kThreads)
     const int e = s_used[ue];
     const int nb = s_cnt[e];
     const int* lst = s_list + s_beg[e];
-    if constexpr (VEC) {
-      float4* h4 = reinterpret_cast<float4*>(home) + (long long)e * nvec;
-      float4* sl4 = reinterpret_cast<float4*>(slot);
-      float4 acc[kVecPerThread];
-      long long idx[kVecPerThread];
+    float* h = home + (long long)e * HHp;
+    Vec<W> acc[kVecPerThread];
+    long long off[kVecPerThread];  // float offset of this thread's vector v in a matrix
+    bool in[kVecPerThread];
 #pragma unroll
-      for (int v = 0; v < kVecPerThread; ++v) {
-        idx[v] = c * per_item + (long long)v * kThreads + tid;
-        acc[v] = idx[v] < nvec ? h4[idx[v]] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      for (int b0 = 0; b0 < nb; b0 += kSlotBatch) {
-        float4 q[kSlotBatch][kVecPerThread];
+    for (int v = 0; v < kVecPerThread; ++v) {
+      const long long i = c * per_item + (long long)v * kThreads + tid;
+      in[v] = i < nvec;
+      off[v] = i * W;
+      if (in[v]) acc[v] = Vec<W>::ld(h + off[v]);
+    }
+    for (int b0 = 0; b0 < nb; b0 += kSlotBatch) {
+      Vec<W> q[kSlotBatch][kVecPerThread];
 #pragma unroll
-        for (int j = 0; j < kSlotBatch; ++j) {
-          if (b0 + j < nb) {
-            const float4* src = sl4 + (long long)lst[b0 + j] * nvec;
+      for (int j = 0; j < kSlotBatch; ++j) {
+        if (b0 + j < nb) {
+          const float* src = slot + (long long)lst[b0 + j] * HHp;
 #pragma unroll
-            for (int v = 0; v < kVecPerThread; ++v)
-              if (idx[v] < nvec) q[j][v] = __ldcs(src + idx[v]);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kSlotBatch; ++j) {
-          if (b0 + j < nb) {
-            float4* dst = sl4 + (long long)lst[b0 + j] * nvec;
-#pragma unroll
-            for (int v = 0; v < kVecPerThread; ++v)
-              if (idx[v] < nvec) {
-                add4(acc[v], q[j][v]);
-                __stcs(dst + idx[v], make_float4(0.f, 0.f, 0.f, 0.f));
-              }
-          }
+          for (int v = 0; v < kVecPerThread; ++v)
+            if (in[v]) q[j][v] = Vec<W>::ld_cs(src + off[v]);
         }
       }
 #pragma unroll
-      for (int v = 0; v < kVecPerThread; ++v)
-        if (idx[v] < nvec) h4[idx[v]] = acc[v];
-    } else {
-      float* h = home + (long long)e * nvec;
+      for (int j = 0; j < kSlotBatch; ++j) {
+        if (b0 + j < nb) {
+          float* dst = slot + (long long)lst[b0 + j] * HHp;
 #pragma unroll
-      for (int v = 0; v < kVecPerThread; ++v) {
-        const long long i = c * per_item + (long long)v * kThreads + tid;
-        if (i >= nvec) continue;
-        float acc = h[i];
-        for (int b = 0; b < nb; ++b) {
-          float* src = slot + (long long)lst[b] * nvec + i;
-          acc = __fadd_rn(acc, *src);
-          *src = 0.f;
+          for (int v = 0; v < kVecPerThread; ++v)
+            if (in[v]) {
+              add_rn(acc[v], q[j][v]);
+              Vec<W>::st_zero_cs(dst + off[v]);
+            }
         }
-        h[i] = acc;
       }
     }
+#pragma unroll
+    for (int v = 0; v < kVecPerThread; ++v)
+      if (in[v]) acc[v].st(h + off[v]);
   }
 }
 
@@ -182,17 +236,23 @@ extern "C" int mep_reduce_grad(const int32_t* slot_expert, int E, int R, int B, 
   if (slot_expert == nullptr || home_grad == nullptr || slot_grad == nullptr)
     return MEP_ERR_INVALID_ARG;
   if (!aligned16(home_grad) || !aligned16(slot_grad)) return MEP_ERR_INVALID_ARG;
-  const bool vec = (HHp % 4) == 0;
+  // widest access the sizes and addresses allow
+  const bool v8 = MEP_REDUCE_V32 && HHp % 8 == 0 && (reinterpret_cast<uintptr_t>(home_grad) & 31u) == 0 &&
+                  (reinterpret_cast<uintptr_t>(slot_grad) & 31u) == 0;
+  const int W = v8 ? 8 : HHp % 4 == 0 ? 4 : 1;
   const int smem = int(sizeof(int)) * (4 * E + 2 + RB);
-  const void* fn = vec ? reinterpret_cast<const void*>(k_reduce_grad<true>)
-                       : reinterpret_cast<const void*>(k_reduce_grad<false>);
+  const void* fn = W == 8   ? reinterpret_cast<const void*>(k_reduce_grad<8>)
+                   : W == 4 ? reinterpret_cast<const void*>(k_reduce_grad<4>)
+                            : reinterpret_cast<const void*>(k_reduce_grad<1>);
   if (set_max_dynamic_smem(fn, smem)) return MEP_ERR_CUDA;
   const int grid = sm_count() * MEP_REDUCE_CTAS_PER_SM;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t err =
-      vec ? launch_pdl(k_reduce_grad<true>, dim3(grid), dim3(kThreads), smem, st, slot_expert, E,
-                       RB, (long long)HHp, home_grad, slot_grad, status)
-          : launch_pdl(k_reduce_grad<false>, dim3(grid), dim3(kThreads), smem, st, slot_expert,
-                       E, RB, (long long)HHp, home_grad, slot_grad, status);
+      W == 8   ? launch_pdl(k_reduce_grad<8>, dim3(grid), dim3(kThreads), smem, st, slot_expert, E,
+                            RB, (long long)HHp, home_grad, slot_grad, status)
+      : W == 4 ? launch_pdl(k_reduce_grad<4>, dim3(grid), dim3(kThreads), smem, st, slot_expert, E,
+                            RB, (long long)HHp, home_grad, slot_grad, status)
+               : launch_pdl(k_reduce_grad<1>, dim3(grid), dim3(kThreads), smem, st, slot_expert, E,
+                            RB, (long long)HHp, home_grad, slot_grad, status);
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }

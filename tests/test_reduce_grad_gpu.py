@@ -77,7 +77,8 @@ def test_reduce_grad_many_slots_per_expert():
     assert (h_got == h_ref).all()
 
 
-@pytest.mark.parametrize("HHp", [1, 3, 1001, 4097])
+# 1, 3, 1001, 4097: single floats; 12, 4100: 16-byte vectors; 4104: 32-byte
+@pytest.mark.parametrize("HHp", [1, 3, 12, 1001, 4097, 4100, 4104])
 def test_reduce_grad_ragged_sizes(HHp):
     E, R, B = 6, 3, 2
     se = np.array([[1, 4], [0, -1], [4, 2]], dtype=np.int32)
@@ -86,6 +87,30 @@ def test_reduce_grad_ragged_sizes(HHp):
     slots = rng.standard_normal((R * B, HHp)).astype(np.float32)
     h_got, h_ref = check(se, home, slots, E)
     assert (h_got == h_ref).all()
+
+
+@pytest.mark.parametrize("shift", [4, 8], ids=["16B_aligned", "32B_aligned"])
+def test_reduce_grad_buffer_alignment(shift):
+    """Buffers that start 16 but not 32 bytes into an allocation take the
+    16-byte path; the result is the same either way."""
+    E, R, B, HHp = 5, 2, 3, 4104
+    se = np.array([[3, 0, -1], [3, 4, 1]], dtype=np.int32)
+    rng = np.random.default_rng(shift)
+    home = rng.standard_normal((E, HHp)).astype(np.float32)
+    slots = rng.standard_normal((R * B, HHp)).astype(np.float32)
+    st_ref, h_ref, s_ref = oracle.reduce_grad(se, home, slots, E)
+    hbuf = torch.zeros(E * HHp + 8, dtype=torch.float32, device=DEV)
+    sbuf = torch.zeros(R * B * HHp + 8, dtype=torch.float32, device=DEV)
+    hd = hbuf[shift:shift + E * HHp].view(E, HHp)
+    sd = sbuf[shift:shift + R * B * HHp].view(R * B, HHp)
+    hd.copy_(to_dev(home))
+    sd.copy_(to_dev(slots))
+    mep.mep_reduce_grad(to_dev(se), hd, sd, None, E)
+    torch.cuda.synchronize()
+    assert st_ref == "ok"
+    np.testing.assert_array_equal(to_np(hd), h_ref)
+    np.testing.assert_array_equal(to_np(sd), s_ref)
+    assert (hbuf[:shift] == 0).all() and (sbuf[shift + R * B * HHp:] == 0).all()
 
 
 def test_reduce_grad_order_fixture_values():
