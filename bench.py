@@ -205,6 +205,37 @@ def whole_job_gbs(world: int, bytes_per_rank: float, max_ms: float) -> float:
 
 
 # ---------------------------------------------------------------------------
+def graph_replay(steps, body, reset, new_events, dev):
+    """The step captured once in a CUDA graph (static shapes, no host sync),
+    then replayed `steps` times with the same untimed reset between replays;
+    returns each replay's CUDA-event time in ms."""
+    import torch
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        reset()
+        body()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    for _ in range(3):
+        reset()
+        graph.replay()
+    events = []
+    for _ in range(steps):
+        reset()
+        e = new_events()
+        e[0].record()
+        graph.replay()
+        e[4].record()
+        events.append(e)
+    torch.cuda.synchronize()
+    return [e[0].elapsed_time(e[4]) for e in events]
+
+
 def gpu_arm(args, rank: int, world: int, dist):
     import torch
 
@@ -256,6 +287,12 @@ def gpu_arm(args, rank: int, world: int, dist):
             e[3].record()
         mep.mep_reduce_grad(plan.slot_expert, home_d, slots_d, plan.status, s.E)
         e[4].record()
+
+    def step_body():
+        mep.mep_plan(idx_d, s.R, s.S, s.K, s.E, s.B, out=plan)
+        mep.mep_dispatch(x_d, plan.dst_pos, plan.status, s.R, s.S, s.K, buf=buf)
+        mep.mep_combine(buf, w_d, plan.dst_pos, plan.status, s.R, s.S, s.K, out=out)
+        mep.mep_reduce_grad(plan.slot_expert, home_d, slots_d, plan.status, s.E)
 
     def untimed_reset():
         # restore the consumed slot gradients, then evict L2 with a > L2 write
@@ -309,6 +346,8 @@ def gpu_arm(args, rank: int, world: int, dist):
         times["combine"].append(e[2].elapsed_time(e[3]))
         times["reduce_grad"].append(e[3].elapsed_time(e[4]))
         times["step_per_kernel_events"].append(e[0].elapsed_time(e[4]))
+    assert int(plan.status.item()) == 0
+    times["graph_step"] = graph_replay(args.steps, step_body, untimed_reset, new_events, dev)
     assert int(plan.status.item()) == 0
 
     nxt = next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp) if rank == 0 else None
@@ -772,9 +811,12 @@ def main():
             "tokens_per_s": round(s.N / ((avg["dispatch"] + avg["combine"]) / 1e3), 0),
             "step_bytes": res["total_bytes"],
             "step_ms_with_per_kernel_events": round(med["step_per_kernel_events"], 4),
+            "graph_replay_ms_per_step": round(avg["graph_step"], 4),
             "note": "per-kernel times from a second run of the same K steps with an event between "
                     "every two kernels (which holds back each programmatic dependent launch); "
-                    "value and ms_per_step come from the timed steps with events at the step ends only",
+                    "value and ms_per_step come from the timed steps with events at the step ends only; "
+                    "graph_replay_ms_per_step: the same step captured once in a CUDA graph and "
+                    "replayed K times (mean), with the same untimed reset between replays",
         },
         "e2e": {"value": round(whole_job_gbs(world, res["total_bytes"], res["e2e_ms"]), 1),
                 "unit": "GB/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
