@@ -664,8 +664,9 @@ def oracle_step_sample(frac: float, seed: int = 0, reps: int = 1) -> dict:
     nb["plan"] = step_bytes(s, HHp, p["slot_expert"])["plan"]
     total = nb["plan"] + nb["dispatch"] + nb["combine"] + nb["reduce_grad"]
     assert out.shape[0] == n_tok and st == "ok"
+    maxvio = float(np.max(p["counts"]) / (s.A / s.E) - 1.0)
     return dict(bytes=total * reps, seconds=tp + td + tc + tr, plan_s=tp, dispatch_s=td,
-                combine_s=tc, reduce_s=tr, frac=frac, n_tok=n_tok, reps=reps)
+                combine_s=tc, reduce_s=tr, frac=frac, n_tok=n_tok, reps=reps, maxvio=maxvio)
 
 
 def cpu_baseline(budget_s: float = 12.0) -> dict:
@@ -709,7 +710,7 @@ def reference_arm(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1000 * tot_s / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(s, None),
+            "config": workload_config(s, r["maxvio"]),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                              "host_cores": len(os.sched_getaffinity(0))
                              if hasattr(os, "sched_getaffinity") else os.cpu_count(),
