@@ -79,6 +79,7 @@ MANUAL = {
     "slots_and_empty": (2, 96, 2, 3, 2, 192, 64, [[0, 70, 70, 150, 192], [30, 30, 31, 31, 192]]),
     "small_buffer": (1, 16, 2, 2, 0, 64, 64, [[5, 32]]),
     "narrow_ragged_n": (1, 64, 2, 1, 0, 128, 72, [[128]]),   # last block: N = 128 MMAs, 72 columns
+    "deep_k": (1, 96, 2, 2, 0, 7168, 136, [[100, 192]]),      # H = 7168: 112 K steps, ragged rows
 }
 
 

@@ -37,6 +37,7 @@ SHAPES = [
     synth.Shape(R=2, E=4, K=1, S=100, H=8, B=2),          # 16-byte rows
     synth.Shape(R=2, E=16, K=10, S=150, H=64, B=8),       # K = 10: generic combine path
     synth.Shape(R=2, E=80, K=40, S=50, H=32, B=40),       # K > 32: two rows per lane
+    synth.Shape(R=4, E=128, K=64, S=24, H=40, B=16),      # K = 64, the limit
 ]
 
 

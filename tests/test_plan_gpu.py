@@ -107,6 +107,9 @@ def test_plan_random_small_sweep():
     (64, 64, 2, 512, 4),      # many ranks
     (3, 20000, 5, 999, 64),   # group sums in their own kernel, one expert per thread (E % 4 != 0)
     (8, 4000, 6, 400, 64),    # group sums in their own kernel, ragged last group of tiles
+    (1024, 16, 2, 1024, 32),  # the most ranks, R * B at the slot limit (1020 slots used)
+    (1024, 32, 8, 2048, 8),   # the most ranks, 1042 slots
+    (1024, 8, 4, 4096, 4),    # the most ranks and experts: capacity error
 ])
 def test_plan_edge_shapes(R, S, K, E, B):
     s = synth.Shape(R=R, E=E, K=K, S=S, H=8, B=B)
