@@ -47,6 +47,7 @@ sys.path.insert(0, ROOT)
 METRIC = "dispatch+combine GB/s & % HBM peak vs maxvio; plan µs; reduce_grad GB/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300's HBM3e, nominal; fractions of it are reported beside the measured ones
 L2_FLUSH_BYTES = 256 << 20
 SWEEP_REPS = 10
 
@@ -553,6 +554,7 @@ def next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp):
 def run_sweep(args, dev, rank):
     """dispatch+combine GB/s across maxvio on the large workload, plus the
     stress routing; plan latency per point."""
+    peak, _ = measured_peak()
     import torch
 
     import load_balancing_topk_gb300 as mep
@@ -613,7 +615,9 @@ def run_sweep(args, dev, rank):
                          dispatch_ms=round(float(np.median(d_only)), 4),
                          combine_ms=round(float(np.median(c_only)), 4),
                          dispatch_combine_ms=round(ms, 4),
-                         dispatch_combine_gbs=round(nbytes / ms / 1e6, 1)))
+                         dispatch_combine_gbs=round(nbytes / ms / 1e6, 1),
+                         frac_of_measured=round(nbytes / ms / 1e6 / peak, 4),
+                         frac_of_nominal=round(nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 4)))
     gbs = [r["dispatch_combine_gbs"] for r in rows if r.get("workload") == "large" and "dispatch_combine_gbs" in r]
     flat = round(max(gbs) / min(gbs), 4) if gbs else None
     del x, buf, out, flush
@@ -798,6 +802,7 @@ def main():
         "config": workload_config(s, res["maxvio"]),
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
                      "traffic": traffic_record(kname),
                      "algorithmic_bytes_per_launch": nb[dom]},
@@ -806,8 +811,11 @@ def main():
             "dispatch_ms": round(med["dispatch"], 4), "combine_ms": round(med["combine"], 4),
             "dispatch_combine_gbs": round(dc_gbs, 1),
             "dispatch_combine_frac_of_peak": round(dc_gbs / peak, 4),
+            "dispatch_combine_frac_of_nominal": round(dc_gbs / NOMINAL_HBM_GBS, 4),
             "reduce_grad_ms": round(med["reduce_grad"], 4),
             "reduce_grad_gbs": round(nb["reduce_grad"] / (avg["reduce_grad"] / 1e3) / 1e9, 1),
+            "reduce_grad_frac_of_nominal": round(
+                nb["reduce_grad"] / (avg["reduce_grad"] / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
             "reduce_grad_slots_used": nb["used"],
             "tokens_per_s": round(s.N / ((avg["dispatch"] + avg["combine"]) / 1e3), 0),
             "step_bytes": res["total_bytes"],
