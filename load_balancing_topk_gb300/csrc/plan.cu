@@ -43,7 +43,16 @@ constexpr int kWarpIters = kTileAssign / (32 * kTileWarps);  // 8 iterations per
 #define MEP_PLAN_THREADS 1024
 #endif
 constexpr int kPlanThreads = MEP_PLAN_THREADS;  // k_plan block size
-constexpr int kMaxScanGroups = 64;           // tile groups in k_plan's prefix pass
+#ifndef MEP_PLAN_SCAN_GROUPS
+#define MEP_PLAN_SCAN_GROUPS 64
+#endif
+constexpr int kMaxScanGroups = MEP_PLAN_SCAN_GROUPS;  // tile groups in k_plan's prefix pass
+#ifndef MEP_PLAN_PRESUM_GROUPS
+#define MEP_PLAN_PRESUM_GROUPS 16
+#endif
+// groups when k_gsum forms them: fewer, longer groups shorten the planner's
+// scan; each k_offsets tile adds its group's earlier tiles before its wait
+constexpr int kPresumGroups = MEP_PLAN_PRESUM_GROUPS;
 constexpr int kPartInts = 8192;              // k_plan shared ints for group sums
 #ifndef MEP_PLAN_GSUM_MIN_INTS
 #define MEP_PLAN_GSUM_MIN_INTS 32768  // tile-count table size (ints) from which k_gsum runs
@@ -61,10 +70,9 @@ struct PlanWs {
   int* groupbase;    // [Gs, E] count of e in all tiles before group g (Gs <= kMaxScanGroups)
   int* groupsum;     // [Gs, E] count of e in group g (k_gsum; large tile tables only)
   int* blockerr;     // [nblk]
-  int* keep;         // [E] tokens kept on the home row
-  int* home_base;    // [E] global row of the home row's first token
-  int* pc_begin;     // [E] first piece of the expert (pieces are grouped by expert)
-  int* pc_count;     // [E]
+  int* etab;         // [E][4] per expert: tokens kept on the home row, global row of
+                     // the home row's first token, first piece (pieces are grouped
+                     // by expert), number of pieces; one 16-byte load in k_offsets
   int* piece_lo;     // [E+R] first list index covered by the piece
   int* piece_base;   // [E+R] global row of the piece's first token
 };
@@ -83,10 +91,7 @@ size_t carve(PlanWs* ws, char* base, int nblk, int R, int E) {
   take(&w->groupbase, size_t(kMaxScanGroups) * E);
   take(&w->groupsum, size_t(kMaxScanGroups) * E);
   take(&w->blockerr, size_t(nblk > 0 ? nblk : 1));
-  take(&w->keep, E);
-  take(&w->home_base, E);
-  take(&w->pc_begin, E);
-  take(&w->pc_count, E);
+  take(&w->etab, size_t(4) * E);
   take(&w->piece_lo, size_t(E) + R);
   take(&w->piece_base, size_t(E) + R);
   return off;
@@ -161,6 +166,7 @@ struct PlanArgs {
   int nblk, R, S, K, E, B;
   int fallback;          // pieces beyond B take the expert's own row instead of failing
   int presummed;         // k_gsum ran: read the group sums, not every tile's counts
+  int Gs, tpg;           // tile groups (tile_groups()) and tiles per group
   int32_t* counts;       // [E]
   int32_t* cu;           // [R, E+B]
   int32_t* slot_expert;  // [R, B]
@@ -204,10 +210,11 @@ __host__ __device__ inline int part_pitch(int Gs) {
   return Gs == 1 ? 1 : ((Gs & 1) ? Gs + 2 : Gs + 1);
 }
 
-// The most groups (<= kMaxScanGroups, <= nblk) whose E rows of part_pitch
-// ints fit kPartInts; E <= MEP_MAX_E = kPartInts / 2 always fits one group.
-__host__ __device__ inline void tile_groups(int nblk, int E, int* Gs, int* tpg) {
-  int g = nblk < kMaxScanGroups ? nblk : kMaxScanGroups;
+// The most groups (<= max_groups <= kMaxScanGroups, <= nblk) whose E rows of
+// part_pitch ints fit kPartInts; E <= MEP_MAX_E = kPartInts / 2 always fits
+// one group.
+inline void tile_groups(int nblk, int E, int max_groups, int* Gs, int* tpg) {
+  int g = nblk < max_groups ? nblk : max_groups;
   while (g > 1 && E * part_pitch(g) > kPartInts) --g;
   if (g < 1) g = 1;
   *Gs = g;
@@ -222,8 +229,7 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT, int* s_e
   using V = typename Vec<W>::T;
   const int E = a.E, nblk = a.nblk, nthr = blockDim.x, tid = threadIdx.x;
   const int nc = E / W;
-  int Gs, tpg;
-  tile_groups(nblk, E, &Gs, &tpg);
+  const int Gs = a.Gs, tpg = a.tpg;
   const int P = part_pitch(Gs);
   const int err0 = tid < nblk ? __ldcg(a.ws.blockerr + tid) : 0;  // in flight with the counts
   if (a.presummed) {
@@ -448,7 +454,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
           ov = T - kp;
           sKeep[e] = kp;
           sOv[e] = ov;
-          a.ws.keep[e] = kp;
+          a.ws.etab[4 * e] = kp;
         }
         const int iO = warp_incl_scan(ov);
         if (e < E) sOst[e] = cO + iO - ov;
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
       sKeep[e] = kp;
       sOv[e] = sT[e] - kp;
       sFlag[e] = sOv[e] > 0 ? 1 : 0;
-      a.ws.keep[e] = kp;
+      a.ws.etab[4 * e] = kp;
     }
     __syncthreads();
     block_excl_scan3(sOv, sOst, sFlag, sFlag, sKeep, sKpre, E, s_warp);
@@ -573,8 +579,8 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   }
   __syncthreads();
   for (int e = tid; e < E; e += nthr) {
-    a.ws.pc_begin[e] = sPcCnt[e] ? sPcBeg[e] : 0;
-    a.ws.pc_count[e] = sPcCnt[e];
+    a.ws.etab[4 * e + 2] = sPcCnt[e] ? sPcBeg[e] : 0;
+    a.ws.etab[4 * e + 3] = sPcCnt[e];
   }
 
   // 5. cu_seqlens; also the global first row of every home row and piece.
@@ -610,7 +616,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   auto write_row = [&](int r, int j, int c, int g, int incl_end) {
     a.cu[size_t(r) * G + j] = incl_end;
     const int start = r * SK + incl_end - c;
-    if (j < E && j / per == r) a.ws.home_base[j] = start;
+    if (j < E && j / per == r) a.ws.etab[4 * j + 1] = start;
     else if (g >= 0) a.ws.piece_base[g] = start;
   };
   if (!s_over) {
@@ -626,7 +632,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
       int c;
       if (j < E) {
         c = j < s0 ? 0 : sKpre[min(j + 1, s0 + per)] - sKpre[s0];
-        if (j >= s0 && j < s0 + per) a.ws.home_base[j] = r * SK + sKpre[j] - sKpre[s0];
+        if (j >= s0 && j < s0 + per) a.ws.etab[4 * j + 1] = r * SK + sKpre[j] - sKpre[s0];
       } else if (j - E < sNp[r]) {
         const int b = j - E, e = sOlist[sQ0[r] + b];
         const int lo = sDst[r], os = sOst[e], oe = os + sOv[e];
@@ -659,18 +665,15 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
 // k_offsets: destination rows.
 __global__ void __launch_bounds__(kTileThreads)
     k_offsets(const int32_t* __restrict__ topk_idx, int N, int K, int E, int R,
-              int tok_per_tile, int nblk, int pieces_smem, PlanWs ws,
+              int tok_per_tile, int tpg, int pieces_smem, PlanWs ws,
               const int32_t* __restrict__ status, int32_t* __restrict__ dst_pos) {
   extern __shared__ int smem[];
   int* s_idx = smem;                          // [kTileAssign]
-  int* s_wcnt = smem + kTileAssign;           // [kTileWarps, E]
-  int* s_keep = s_wcnt + kTileWarps * E;      // [E]
-  int* s_hb = s_keep + E;                     // [E]
-  int* s_pcb = s_hb + E;                      // [E] first piece of the expert
-  int* s_pcn = s_pcb + E;                     // [E] pieces of the expert
+  int* s_wcnt = smem + kTileAssign;           // [kTileWarps, E]; after the wait, the row tables
+  int* s_pc = s_wcnt + kTileWarps * E;        // piece tables, when they fit (pieces_smem)
   // piece tables: in shared memory when they fit (pieces_smem), else global
-  const int* s_plo = pieces_smem ? s_pcn + E : ws.piece_lo;          // [E+R]
-  const int* s_pbase = pieces_smem ? s_pcn + 2 * E + R : ws.piece_base;  // [E+R]
+  const int* s_plo = pieces_smem ? s_pc : ws.piece_lo;             // [E+R]
+  const int* s_pbase = pieces_smem ? s_pc + E + R : ws.piece_base;  // [E+R]
   const int blk = blockIdx.x;
   const int t0 = blk * tok_per_tile;
   const int ntok = min(tok_per_tile, N - t0);
@@ -724,8 +727,6 @@ __global__ void __launch_bounds__(kTileThreads)
   // group's earlier tiles come from k_hist, which has completed before this
   // grid can start (the planner releases it only after its own wait on
   // k_hist). Then each assignment's expert and offset go to registers.
-  int Gs, tpg;
-  tile_groups(nblk, E, &Gs, &tpg);
   const int g = blk / tpg;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
@@ -753,18 +754,22 @@ __global__ void __launch_bounds__(kTileThreads)
   pdl_wait();                           // the planner's tables and status
   pdl_launch_dependents();
   const int st = status != nullptr ? __ldcg(status) : 0;
-  int* s_gb = s_wcnt;                   // [E] the group's base, per expert
+  // Per expert, with this group's base gb folded in: a kept token's row is
+  // home_base + gb + rel, for rel < keep - gb (one 8-byte shared load on the
+  // common path); the rest go through the expert's pieces.
+  int2* s_fast = reinterpret_cast<int2*>(s_wcnt);  // [E] {home_base + gb, keep - gb}
+  int2* s_slow = s_fast + E;                       // [E] {gb, first piece | pieces << 16}
+  const int4* etab = reinterpret_cast<const int4*>(ws.etab);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    s_gb[e] = __ldcg(ws.groupbase + size_t(g) * E + e);
-    s_keep[e] = __ldcg(ws.keep + e);
-    s_hb[e] = __ldcg(ws.home_base + e);
-    s_pcb[e] = __ldcg(ws.pc_begin + e);
-    s_pcn[e] = __ldcg(ws.pc_count + e);
+    const int gb = __ldcg(ws.groupbase + size_t(g) * E + e);
+    const int4 t = __ldcg(etab + e);
+    s_fast[e] = make_int2(t.y + min(gb, t.x), t.x - gb);  // (no kept token left: unused base)
+    s_slow[e] = make_int2(gb, t.z | (t.w << 16));
   }
   if (pieces_smem)
     for (int q = threadIdx.x; q < E + R; q += blockDim.x) {
-      s_pcn[E + q] = __ldcg(ws.piece_lo + q);
-      s_pcn[2 * E + R + q] = __ldcg(ws.piece_base + q);
+      s_pc[q] = __ldcg(ws.piece_lo + q);
+      s_pc[E + R + q] = __ldcg(ws.piece_base + q);
     }
   if (st != 0) return;                  // uniform: one status word
   __syncthreads();
@@ -774,15 +779,20 @@ __global__ void __launch_bounds__(kTileThreads)
     const int a = wbeg + j * 32 + lane;
     if (a < wend) {
       const int e = ej[j];
-      const int i = s_gb[e] + rel[j];   // index of the token in expert e's list
+      const int2 f = s_fast[e];
       int row;
-      if (i < s_keep[e]) {
-        row = s_hb[e] + i;
+      if (rel[j] < f.y) {
+        row = f.x + rel[j];
       } else {
-        const int p0 = s_pcb[e], pn = s_pcn[e];
-        int p = p0;
-        for (int q = p0 + 1; q < p0 + pn; ++q)
-          if (s_plo[q] <= i) p = q;
+        const int2 sl = s_slow[e];
+        const int i = sl.x + rel[j];    // index of the token in expert e's list
+        // the expert's pieces are consecutive and their first list indices
+        // ascend: the last piece starting at or before i holds the token
+        int p = sl.y & 0xffff, hi = p + (sl.y >> 16) - 1;
+        while (p < hi) {
+          const int m = (p + hi + 1) >> 1;
+          if (s_plo[m] <= i) p = m; else hi = m - 1;
+        }
         row = s_pbase[p] + (i - s_plo[p]);
       }
       out[a] = row;
@@ -841,7 +851,7 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
   const int hist_smem = E * int(sizeof(int));
   // k_offsets keeps its tile, per-warp counters and per-expert tables in
   // shared memory, and the piece tables too when all of it fits
-  const int offs_base = (kTileAssign + (kTileWarps + 4) * E) * int(sizeof(int));
+  const int offs_base = (kTileAssign + kTileWarps * E) * int(sizeof(int));
   const int offs_pieces = 2 * (E + R) * int(sizeof(int));
   const int pieces_smem = offs_base + offs_pieces <= 220 * 1024 ? 1 : 0;
   const int offs_smem = offs_base + (pieces_smem ? offs_pieces : 0);
@@ -855,9 +865,10 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
   if (nblk > 0) k_hist<<<nblk, kTileThreads, hist_smem, st>>>(topk_idx, N, K, E, tpt, ws);
   // Beyond 128 KB of tile counts, the group sums are formed by Gs CTAs in
   // parallel rather than inside the one planner CTA.
+  const bool big = (long long)nblk * E >= MEP_PLAN_GSUM_MIN_INTS;
   int Gs, tpg;
-  tile_groups(nblk, E, &Gs, &tpg);
-  const int presum = (long long)nblk * E >= MEP_PLAN_GSUM_MIN_INTS && Gs > 1 ? 1 : 0;
+  tile_groups(nblk, E, big ? kPresumGroups : kMaxScanGroups, &Gs, &tpg);
+  const int presum = big && Gs > 1 ? 1 : 0;
   if (presum) {
     const cudaError_t e =
         (E & 3) == 0
@@ -867,13 +878,13 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
                          static_cast<const int*>(ws.blockhist), nblk, E, tpg, ws.groupsum);
     if (e != cudaSuccess) return MEP_ERR_CUDA;
   }
-  PlanArgs pa{nblk,        R,         S,           K,      E, B, fallback, presum,
+  PlanArgs pa{nblk,          R,          S,           K,      E,  B, fallback, presum, Gs, tpg,
               expert_counts, cu_seqlens, slot_expert, status, ws};
   if (launch_pdl(k_plan, dim3(1), dim3(kPlanThreads), plan_smem, st, pa) != cudaSuccess)
     return MEP_ERR_CUDA;
   if (nblk > 0 &&
       launch_pdl(k_offsets, dim3(nblk), dim3(kTileThreads), offs_smem, st, topk_idx, N, K, E, R,
-                 tpt, nblk, pieces_smem, ws, static_cast<const int32_t*>(status),
+                 tpt, tpg, pieces_smem, ws, static_cast<const int32_t*>(status),
                  dst_pos) != cudaSuccess)
     return MEP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
