@@ -524,20 +524,22 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     int np = 0, q0 = 0;
     const int d = sDef[r];
     if (d > 0) {
+      // the segments tile the overflow line in order, so the ones meeting
+      // [lo, hi) are those from the first ending after lo up to (not
+      // including) the first starting at or after hi: two binary searches
       const int lo = sDst[r], hi = lo + d;
-      int q1 = nov;  // first q whose segment ends after lo
+      int q1 = nov;
       while (q0 < q1) {
         const int m = (q0 + q1) >> 1;
         const int e = sOlist[m];
         if (sOst[e] + sOv[e] > lo) q1 = m; else q0 = m + 1;
       }
-      for (int q = q0; q < nov; ++q) {
-        const int e = sOlist[q];
-        const int os = sOst[e], oe = os + sOv[e];
-        if (max(os, lo) >= min(oe, hi)) break;
-        ++np;
-        if (min(oe, hi) < oe) break;
+      int q2 = q0, q3 = nov;
+      while (q2 < q3) {
+        const int m = (q2 + q3) >> 1;
+        if (sOst[sOlist[m]] >= hi) q3 = m; else q2 = m + 1;
       }
+      np = q2 - q0;
     }
     if (np > B) {
       if (!a.fallback) s_cap = 1;
