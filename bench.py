@@ -9,11 +9,13 @@ tensors whose slot map is that step's plan.
 The timed region records CUDA events at the step ends only, so every kernel's
 programmatic dependent launch overlaps its predecessor as in use; a second run
 of the same steps with an event between every two kernels gives the per-kernel
-breakdown and the roofline kernel's duration.
+breakdown and the roofline kernel's duration; a third run replays the same
+step from one captured CUDA graph.
 
 Printed (one JSON line, rank 0): whole-step GB/s of algorithmic bytes, the
 per-step breakdown (plan us, dispatch+combine GB/s, reduce_grad GB/s), the
-roofline of the dominant kernel against the measured HBM copy peak, an
+roofline of the dominant kernel against the measured HBM copy peak (and the
+nominal 7.9 TB/s), the next rows (prefetch, backward, grouped GEMM), an
 end-to-end figure through the public API with host buffers, the CPU oracle
 on a bounded sample, SM clocks sampled during the timed region, and a
 maxvio sweep of dispatch+combine on the R=8 / E=256 / K=8 / S=8192 /
