@@ -57,6 +57,9 @@ constexpr int kPartInts = 8192;              // k_plan shared ints for group sum
 #ifndef MEP_PLAN_GSUM_MIN_INTS
 #define MEP_PLAN_GSUM_MIN_INTS 32768  // tile-count table size (ints) from which k_gsum runs
 #endif
+#ifndef MEP_PLAN_RANK_WARPS
+#define MEP_PLAN_RANK_WARPS 1  // keep / overflow by one warp per rank where E/R <= 32 and R <= 32
+#endif
 #ifndef MEP_PLAN_WARP_SCAN_MAX_E
 #define MEP_PLAN_WARP_SCAN_MAX_E 128
 #endif
@@ -437,7 +440,63 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   //    beyond, block-wide scans (faster on GB300 from E = 256 on).
   // (the group sums are consumed: sPart now holds the running sum of keep)
   int* sKpre = sPart;  // [E+1] exclusive prefix of keep, total at E
-  if (E <= MEP_PLAN_WARP_SCAN_MAX_E) {
+  if (MEP_PLAN_RANK_WARPS && per <= 32 && R <= nwarps) {
+    // Warp r holds rank r's home experts, one per lane: the keep, overflow,
+    // flag and keep prefixes inside the rank are warp scans, and the rank's
+    // load gives its deficit. Warp 0 then scans the R rank totals (and the
+    // deficits), and each warp adds its rank's offsets: two block barriers.
+    const int r = warp, e = r * per + lane;
+    const bool in = r < R && lane < per;
+    int ov = 0, f = 0, kp = 0, exO = 0, exF = 0, exK = 0;
+    if (r < R) {
+      const int T = in ? sT[e] : 0;
+      const int iT = warp_incl_scan(T);
+      kp = in ? max(0, min(T, SK - (iT - T))) : 0;
+      ov = T - kp;
+      f = ov > 0 ? 1 : 0;
+      const int iO = warp_incl_scan(ov), iF = warp_incl_scan(f), iK = warp_incl_scan(kp);
+      exO = iO - ov;
+      exF = iF - f;
+      exK = iK - kp;
+      if (in) {
+        sKeep[e] = kp;
+        sOv[e] = ov;
+        a.ws.etab[4 * e] = kp;
+      }
+      if (lane == 31) {
+        s_warp[r] = iO;
+        s_warp[33 + r] = iF;
+        s_warp[66 + r] = iK;
+        sDef[r] = max(0, SK - iT);  // iT at lane 31: the rank's load
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int v = lane < R ? s_warp[33 * q + lane] : 0;
+        const int vi = warp_incl_scan(v);
+        s_warp[33 * q + lane] = vi - v;
+        if (lane == 31) s_warp[33 * q + 32] = vi;
+      }
+      const int d = lane < R ? sDef[lane] : 0;
+      const int iD = warp_incl_scan(d);
+      if (lane < R) sDst[lane] = iD - d;
+      if (lane == 31) sDst[R] = iD;
+    }
+    __syncthreads();
+    if (in) {
+      sOst[e] = s_warp[r] + exO;
+      if (f) sOlist[s_warp[33 + r] + exF] = e;
+      sKpre[e] = s_warp[66 + r] + exK;
+    }
+    if (tid == 0) {
+      sOst[E] = s_warp[32];
+      sFlag[E] = s_warp[65];
+      sKpre[E] = s_warp[98];
+    }
+    __syncthreads();
+  } else if (E <= MEP_PLAN_WARP_SCAN_MAX_E) {
     if (warp == 0) {
       int cT = 0, cO = 0, cF = 0, cK = 0;
       for (int e0 = 0; e0 < E; e0 += 32) {
