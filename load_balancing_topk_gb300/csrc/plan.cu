@@ -435,9 +435,10 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   // 2. home-first keep: the count of e's earlier home experts is a
   //    difference of the running sum of T; then
   // 3. overflow segments (expert order) and deficits (rank order) on one
-  //    line. Up to 128 experts, warp 0 does both in one pass over chunks
-  //    of 32 experts (three warp scans per chunk, no block barrier);
-  //    beyond, block-wide scans (faster on GB300 from E = 256 on).
+  //    line. Where E/R <= 32 and R <= 32, one warp per rank (below);
+  //    otherwise, up to 128 experts, warp 0 does both in one pass over
+  //    chunks of 32 experts (three warp scans per chunk, no block barrier),
+  //    and beyond, block-wide scans (faster on GB300 from E = 256 on).
   // (the group sums are consumed: sPart now holds the running sum of keep)
   int* sKpre = sPart;  // [E+1] exclusive prefix of keep, total at E
   if (MEP_PLAN_RANK_WARPS && per <= 32 && R <= nwarps) {
