@@ -12,9 +12,10 @@
 // dispatch: each token row is read from HBM once and written K times. One
 //   warp per token: every lane loads 8 coalesced 32-byte vectors of the row
 //   (16-byte ones when H % 16 != 0 or a pointer is not 32-byte aligned) and
-//   stores each to the K destination rows with streaming stores; 16 CTAs
-//   of 8 warps per SM keep enough stores in flight to run at the HBM write
-//   rate. (A design that staged rows in shared memory with
+//   stores each to the K destination rows with streaming stores. CTAs of 8
+//   warps, up to 64 per SM before the warps loop (one token per warp up to
+//   9728 CTAs on 152 SMs): a wave of fresh CTAs keeps enough stores in
+//   flight to run at the HBM write rate. (A design that staged rows in shared memory with
 //   cp.async.bulk and wrote them back with K bulk stores per row measured
 //   4-8% slower on GB300, at 4 KB and at 14 KB rows.)
 // combine: one warp per token; each lane owns 16-byte column vectors and
@@ -37,10 +38,13 @@
 #define MEP_DISPATCH_V32 1
 #endif
 #ifndef MEP_DISPATCH_CTAS_PER_SM
-#define MEP_DISPATCH_CTAS_PER_SM 16
+#define MEP_DISPATCH_CTAS_PER_SM 64
 #endif
 #ifndef MEP_COMBINE_WARPS
 #define MEP_COMBINE_WARPS 4
+#endif
+#ifndef MEP_COMBINE_CTAS_PER_SM
+#define MEP_COMBINE_CTAS_PER_SM 64
 #endif
 
 namespace mep {
@@ -60,7 +64,7 @@ constexpr int kCombineUnroll = MEP_COMBINE_UNROLL;      // 16-byte column vector
 constexpr int kCombineUnroll32 = MEP_COMBINE_UNROLL32;  // 32-byte column vectors per lane in flight
 
 
-// One warp per token (grid-stride). Each lane holds kUnroll vectors
+// One warp per token (grid-stride past the grid cap). Each lane holds kUnroll vectors
 // of the row and writes each to the K destination rows with streaming
 // (evict-first) stores: the buffer is written once here and read back by the
 // expert computation, not by this kernel. KT > 0: K fixed at compile time,
@@ -251,7 +255,7 @@ cudaError_t launch_combine(const void* y, const float* w, const int32_t* dst, in
                            long long N, int K, int H, long long nrows, void* out,
                            cudaStream_t st) {
   const long long want = (N + MEP_COMBINE_WARPS - 1) / MEP_COMBINE_WARPS;
-  const long long cap = (long long)sm_count() * 64;
+  const long long cap = (long long)sm_count() * MEP_COMBINE_CTAS_PER_SM;
   const int grid = int(want < cap ? want : cap);
   if (MEP_COMBINE_V32 && H % 16 == 0 && aligned32(y) && aligned32(out))
     return launch_pdl(k_combine<KT, UNIT, Vec32>, dim3(grid), dim3(32 * MEP_COMBINE_WARPS), 0,
