@@ -21,6 +21,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVec = 4;  // 16-byte vectors per thread per item
+#ifndef MEP_PREFETCH_CTAS_PER_SM
+#define MEP_PREFETCH_CTAS_PER_SM 16
+#endif
 
 __global__ void __launch_bounds__(kThreads)
     k_prefetch(const int32_t* __restrict__ slot_expert, int E, int RB, long long nvec,
@@ -93,7 +96,7 @@ extern "C" int mep_prefetch(const int32_t* slot_expert, int E, int R, int B, int
   if (!aligned16(home_w) || !aligned16(slot_w)) return MEP_ERR_INVALID_ARG;
   const int smem = int(sizeof(int)) * RB;
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_prefetch), smem)) return MEP_ERR_CUDA;
-  const int grid = sm_count() * 8;
+  const int grid = sm_count() * MEP_PREFETCH_CTAS_PER_SM;
   const cudaError_t err =
       launch_pdl(k_prefetch, dim3(grid), dim3(kThreads), smem, static_cast<cudaStream_t>(stream),
                  slot_expert, E, RB, (long long)(expert_bytes / 16),
