@@ -64,13 +64,14 @@ constexpr int kCombineUnroll = MEP_COMBINE_UNROLL;      // 16-byte column vector
 constexpr int kCombineUnroll32 = MEP_COMBINE_UNROLL32;  // 32-byte column vectors per lane in flight
 
 
-// One warp per token (grid-stride past the grid cap). Each lane holds kUnroll vectors
-// of the row and writes each to the K destination rows with streaming
-// (evict-first) stores: the buffer is written once here and read back by the
-// expert computation, not by this kernel. KT > 0: K fixed at compile time,
-// destination offsets held in registers; KT == 0: any K, offsets re-read
-// per vector (L1 hits).
-template <int KT, typename V>
+// One warp per token (grid-stride past the grid cap). Each lane holds U
+// vectors of the row (U = 16 for rows longer than 8 vectors per lane, so that
+// a 7168-wide row moves in one round) and writes each to the K destination
+// rows with streaming (evict-first) stores: the buffer is written once here
+// and read back by the expert computation, not by this kernel. KT > 0: K
+// fixed at compile time, destination offsets held in registers; KT == 0: any
+// K, offsets re-read per vector (L1 hits).
+template <int KT, typename V, int U>
 __global__ void __launch_bounds__(32 * MEP_DISPATCH_WARPS)
     k_dispatch(const V* __restrict__ hidden, const int32_t* __restrict__ dst_pos,
                int32_t* status, long long N, int Kr, long long vpr, long long nrows,
@@ -96,32 +97,32 @@ __global__ void __launch_bounds__(32 * MEP_DISPATCH_WARPS)
         const int r = __shfl_sync(MEP_FULL_MASK, r0, k);
         off[k] = (r >= 0 && r < nrows) ? (long long)r * vpr : -1;
       }
-      for (long long v0 = lane; v0 < vpr; v0 += 32 * kUnroll) {
-        V q[kUnroll];
+      for (long long v0 = lane; v0 < vpr; v0 += 32 * U) {
+        V q[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
+        for (int u = 0; u < U; ++u)
           if (v0 + 32 * u < vpr) q[u] = ld_nc(src + v0 + 32 * u);
 #pragma unroll
         for (int k = 0; k < KT; ++k) {
           if (off[k] < 0) continue;
           V* o = buf + off[k] + v0;
 #pragma unroll
-          for (int u = 0; u < kUnroll; ++u)
+          for (int u = 0; u < U; ++u)
             if (v0 + 32 * u < vpr) st_cs(o + 32 * u, q[u]);
         }
       }
     } else {
-      for (long long v0 = lane; v0 < vpr; v0 += 32 * kUnroll) {
-        V q[kUnroll];
+      for (long long v0 = lane; v0 < vpr; v0 += 32 * U) {
+        V q[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
+        for (int u = 0; u < U; ++u)
           if (v0 + 32 * u < vpr) q[u] = ld_nc(src + v0 + 32 * u);
         for (int k = 0; k < K; ++k) {
           const int r = __ldg(dst_pos + t * K + k);
           if (r < 0 || r >= nrows) continue;
           V* o = buf + (long long)r * vpr + v0;
 #pragma unroll
-          for (int u = 0; u < kUnroll; ++u)
+          for (int u = 0; u < U; ++u)
             if (v0 + 32 * u < vpr) st_cs(o + 32 * u, q[u]);
         }
       }
@@ -135,11 +136,17 @@ cudaError_t launch_dispatch(const void* x, const int32_t* dst, int32_t* status, 
   const long long want = (N + MEP_DISPATCH_WARPS - 1) / MEP_DISPATCH_WARPS;
   const long long cap = (long long)sm_count() * MEP_DISPATCH_CTAS_PER_SM;
   const int grid = int(want < cap ? want : cap);
-  if (MEP_DISPATCH_V32 && H % 16 == 0 && aligned32(x) && aligned32(buf))
-    return launch_pdl(k_dispatch<KT, Vec32>, dim3(grid), dim3(32 * MEP_DISPATCH_WARPS), 0, st,
-                      static_cast<const Vec32*>(x), dst, status, N, K, (long long)(H / 16), nrows,
+  if (MEP_DISPATCH_V32 && H % 16 == 0 && aligned32(x) && aligned32(buf)) {
+    const long long vpr = H / 16;
+    if (vpr > 32 * kUnroll)
+      return launch_pdl(k_dispatch<KT, Vec32, 2 * kUnroll>, dim3(grid), dim3(32 * MEP_DISPATCH_WARPS),
+                        0, st, static_cast<const Vec32*>(x), dst, status, N, K, vpr, nrows,
+                        static_cast<Vec32*>(buf));
+    return launch_pdl(k_dispatch<KT, Vec32, kUnroll>, dim3(grid), dim3(32 * MEP_DISPATCH_WARPS), 0,
+                      st, static_cast<const Vec32*>(x), dst, status, N, K, vpr, nrows,
                       static_cast<Vec32*>(buf));
-  return launch_pdl(k_dispatch<KT, uint4>, dim3(grid), dim3(32 * MEP_DISPATCH_WARPS), 0, st,
+  }
+  return launch_pdl(k_dispatch<KT, uint4, kUnroll>, dim3(grid), dim3(32 * MEP_DISPATCH_WARPS), 0, st,
                     static_cast<const uint4*>(x), dst, status, N, K, (long long)(H / 8), nrows,
                     static_cast<uint4*>(buf));
 }
