@@ -38,6 +38,7 @@ SHAPES = [
     synth.Shape(R=2, E=16, K=10, S=150, H=64, B=8),       # K = 10: generic combine path
     synth.Shape(R=2, E=80, K=40, S=50, H=32, B=40),       # K > 32: two rows per lane
     synth.Shape(R=4, E=128, K=64, S=24, H=40, B=16),      # K = 64, the limit
+    synth.Shape(R=2, E=8, K=4, S=96, H=4160, B=4),        # 260 32-byte vectors a row: 16 per lane, ragged
 ]
 
 
