@@ -189,8 +189,11 @@ MEP_API int mep_prefetch(const int32_t* slot_expert, int E, int R, int B, int64_
  *     before anything is enqueued.
  *   - No cudaMalloc, cudaFree or allocating library call is made.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture. MEP_ERR_CUDA if the lookup fails.
+ *     (cudaGetSymbolAddress) with that device current, and caches it with
+ *     the id of the current CUDA context; make that first call before any
+ *     stream capture. A call in a new context of the device (after
+ *     cudaDeviceReset) looks the address up again: after a reset, make one
+ *     call before any capture again. MEP_ERR_CUDA if the lookup fails.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents (each call writes every scratch byte it later reads, so no
  *     clearing is needed). Calls that overlap on the GPU -- on different
@@ -325,7 +328,9 @@ MEP_API int mep_reduce_grad(const int32_t* slot_expert, int E, int R, int B, int
  *   y          bf16 [R*S*K, H']      output, every row written; must not overlap
  *              the inputs
  * Host returns: MEP_OK, MEP_ERR_INVALID_ARG (sizes, null pointers, alignment:
- * every tensor 16-byte aligned), MEP_ERR_CUDA.
+ * every tensor 16-byte aligned; x, w_home, w_slot and y must be device memory
+ * of the current device, since the kernel's tensor-core operands are copied
+ * through tensor maps encoded over them), MEP_ERR_CUDA.
  */
 MEP_API int mep_grouped_gemm_workspace_bytes(int R, int S, int K, int E, int B, size_t* bytes);
 MEP_API int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens, const mep_bf16* w_home,

@@ -33,11 +33,6 @@
 //                 stores of the valid rows and columns, then a release on CTA 0's
 //                 accumulator barrier; the accumulator is double-buffered,
 //                 so the next unit's MMAs overlap this store.
-//   k_gemm<CL>    the same pipeline with 1-SM MMAs (M = 128): for CL = 2 the
-//                 two CTAs of a cluster share the weight tile by TMA
-//                 multicast (4-stage ring of 48 KB); for CL = 1 every CTA
-//                 loads its own. Selected by MEP_GEMM_PAIR_MMA=0 or
-//                 MEP_GEMM_CLUSTER=1 at build time.
 // Every wait is bounded (MEP_GEMM_TIMEOUT_NS on %globaltimer): a wait that
 // gives up raises a CTA-wide abort flag and MEP_ERR_TIMEOUT; every role then
 // leaves its loop, the producer waits for its own copies in flight, the MMA
@@ -56,12 +51,6 @@
 #ifndef MEP_GEMM_B_SBO
 #define MEP_GEMM_B_SBO 1024  // byte stride between 8-row K groups of a weight stage
 #endif
-#ifndef MEP_GEMM_CLUSTER
-#define MEP_GEMM_CLUSTER 2  // CTAs sharing one weight tile (1 or 2)
-#endif
-#ifndef MEP_GEMM_PAIR_MMA
-#define MEP_GEMM_PAIR_MMA 1  // clusters of 2 run k_gemm_pair (cta_group::2 MMAs)
-#endif
 #ifndef MEP_GEMM_NARROW_N
 #define MEP_GEMM_NARROW_N 1  // a last column block of <= 128 columns runs N = 128 pair MMAs
 #endif
@@ -78,14 +67,12 @@ namespace {
 constexpr int kBM = 128;                   // tile rows (TMEM lanes)
 constexpr int kBN = 256;                   // tile columns of H' (TMEM columns per accumulator)
 constexpr int kBK = 64;                    // K step: one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;     // 16 KB
 constexpr int kBBox = kBK * 64 * 2;        // one 64x64 weight box, 8 KB
-constexpr int kBBytes = 4 * kBBox;         // 32 KB
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 2 * kBN;         // double-buffered accumulator
 constexpr int kTileThreads = 1024;
-constexpr int kSmemBytes = 1024 /* alignment slack */ + kStages * (kABytes + kBBytes) + 256;
+constexpr int kPair = 2;                   // CTAs per cluster (one CTA pair)
 
 // ---------------------------------------------------------------------------
 // PTX wrappers (mbarrier, TMA, tcgen05)
@@ -149,27 +136,6 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   return wait_phase_slow(bar, parity, abort, status, honor_abort);
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// The same load, landing at the same shared-memory offset (and completing
-// bytes on the mbarrier at the same offset) in every CTA of the cluster
-// named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                               uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // cta_group::2 form: the data lands in this CTA's shared memory, the bytes
 // are counted on an mbarrier that may sit in the peer CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -215,36 +181,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
          ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and
-// B bf16 (bits 7-9 = 1, 10-12 = 1), A K-major (bit 15 = 0), B MN-major
-// (bit 16 = 1), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
-                            ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// Arrive on the mbarrier at this offset in every CTA of cta_mask once this
-// thread's MMAs so far have completed.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
 }
 
 // The pair form: M = 256 rows over the two CTAs of a pair (each CTA's 128
@@ -407,196 +343,9 @@ struct GemmSmem {
   int count;
 };
 
-template <int CL>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_gemm(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wh,
-           const __grid_constant__ CUtensorMap map_ws, const int4* __restrict__ tiles,
-           const int* __restrict__ count_ptr, int32_t* status, int E, int H, int Hp,
-           __nv_bfloat16* __restrict__ y, int st32_flag) {
-  static_assert(CL == 1 || CL == 2, "clusters of 1 or 2 CTAs");
-  const bool st32 = st32_flag != 0;
-  constexpr uint16_t kMask = (1u << CL) - 1u;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzled stages want 1024-byte alignment
-  uint8_t* gen_base = smem_raw + (base - raw);
-  const uint32_t sa = base;                      // A stages
-  const uint32_t sb = base + kStages * kABytes;  // B stages
-  GemmSmem* S = reinterpret_cast<GemmSmem*>(gen_base + kStages * (kABytes + kBBytes));
-  volatile int* abort_flag = &S->abort;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = CL > 1 ? int(cluster_rank()) : 0;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&S->full[s]), 1);
-      mbar_init(smem_u32(&S->empty[s]), CL);  // one MMA commit from every CTA of the cluster
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(smem_u32(&S->tfull[a]), 1);
-      mbar_init(smem_u32(&S->tempty[a]), 4);
-    }
-    mbar_init(smem_u32(&S->drain), 1);
-    S->abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&S->tmem)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  pdl_wait();
-  if (threadIdx.x == 0) S->count = read_status(status) != 0 ? 0 : *count_ptr;
-  tc_fence_before();
-  __syncthreads();
-  // the peer multicasts into this CTA's ring only after its barriers exist
-  if (CL > 1) cluster_sync();
-  tc_fence_after();
-  const uint32_t tmem = S->tmem;
-  const int nN = (Hp + kBN - 1) / kBN;
-  // work units of the cluster: (pair of adjacent tiles, column block); CTA
-  // `rank` of the cluster takes tile CL * pair + rank
-  const long long units = (long long)(S->count / CL) * nN;
-  const long long u0 = blockIdx.x / CL, ustep = gridDim.x / CL;
-  const int nk = H / kBK;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      uint32_t it = 0;
-      int last_round[kStages];
-      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
-      bool ok = true;
-      for (long long u = u0; ok && u < units; u += ustep) {
-        const int4 t = tiles[(u / nN) * CL + rank];
-        const int n0 = int(u % nN) * kBN;
-        const bool home = t.z < E;
-        const CUtensorMap* wmap = home ? &map_wh : &map_ws;
-        const int wrow = (home ? t.z : t.z - E) * H;
-        const int left = (Hp - n0 + 63) / 64;
-        const int nbox = left < 4 ? left : 4;
-        const uint32_t bytes = kABytes + nbox * kBBox;  // every box lands in every CTA
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = int(it % kStages);
-          const uint32_t round = it / kStages;
-          if (!wait_phase(smem_u32(&S->empty[s]), (round & 1u) ^ 1u, abort_flag, status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = smem_u32(&S->full[s]);
-          mbar_expect_tx(fb, bytes);
-          tma_load_2d(sa + s * kABytes, &map_x, kb * kBK, t.x, fb);
-          for (int i = rank; i < nbox; i += CL) {
-            if (CL > 1)
-              tma_load_2d_mc(sb + s * kBBytes + i * kBBox, wmap, n0 + 64 * i, wrow + kb * kBK, fb,
-                             kMask);
-            else
-              tma_load_2d(sb + s * kBBytes + i * kBBox, wmap, n0 + 64 * i, wrow + kb * kBK, fb);
-          }
-          last_round[s] = int(round);
-        }
-      }
-      // before the CTA may exit: its ring has received every copy it asked
-      // for, and (cluster) every MMA commit aimed at its stage barriers
-      for (int s = 0; s < kStages; ++s)
-        if (last_round[s] >= 0) {
-          wait_phase(smem_u32(&S->full[s]), uint32_t(last_round[s]) & 1u, abort_flag, status,
-                     false);
-          if (CL > 1)
-            wait_phase(smem_u32(&S->empty[s]), uint32_t(last_round[s]) & 1u, abort_flag, status,
-                       false);
-        }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      uint32_t it = 0, lt = 0;
-      bool ok = true;
-      for (long long u = u0; ok && u < units; u += ustep, ++lt) {
-        const uint32_t a = lt & 1u, use = lt >> 1;
-        if (!wait_phase(smem_u32(&S->tempty[a]), (use & 1u) ^ 1u, abort_flag, status)) break;
-        tc_fence_after();
-        const uint32_t d = tmem + a * kBN;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = int(it % kStages);
-          if (!wait_phase(smem_u32(&S->full[s]), (it / kStages) & 1u, abort_flag, status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // A: K-major, 16 elements = 32 bytes further along the swizzled row.
-            const uint64_t ad = sdesc(sa + s * kABytes + kk * 32, 16, 1024);
-            // B: MN-major, 16 K rows = 2 groups of 8 rows further down.
-            const uint64_t bd =
-                sdesc(sb + s * kBBytes + kk * 16 * 128, MEP_GEMM_B_LBO, MEP_GEMM_B_SBO);
-            tc_mma(d, ad, bd, (kb | kk) != 0 ? 1u : 0u);
-          }
-          // the stage is free in every CTA of the cluster once all their MMAs read it
-          if (CL > 1)
-            tc_commit_mc(smem_u32(&S->empty[s]), kMask);
-          else
-            tc_commit(smem_u32(&S->empty[s]));
-        }
-        if (!ok) break;
-        tc_commit(smem_u32(&S->tfull[a]));
-      }
-      // every MMA this thread issued has completed once `drain` flips
-      tc_commit(smem_u32(&S->drain));
-      wait_phase(smem_u32(&S->drain), 0u, abort_flag, status, false);
-    }
-    __syncwarp();
-  } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const int q = warp & 3;  // this warp may read TMEM lanes [32q, 32q + 32)
-    uint32_t lt = 0;
-    for (long long u = u0; u < units; u += ustep, ++lt) {
-      const uint32_t a = lt & 1u, use = lt >> 1;
-      if (!wait_phase(smem_u32(&S->tfull[a]), use & 1u, abort_flag, status)) break;
-      tc_fence_after();
-      const int4 t = tiles[(u / nN) * CL + rank];
-      const int n0 = int(u % nN) * kBN;
-      const int r = 32 * q + lane;
-      const bool row_ok = r < t.y;  // padding tiles have no rows
-      __nv_bfloat16* out = y + ((long long)t.x + r) * Hp + n0;
-      for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
-        uint32_t v[32];
-        tc_ld32(tmem + a * kBN + 32 * c + ((uint32_t)(32 * q) << 16), v);
-        if (row_ok) store_chunk(out + 32 * c, v, Hp - (n0 + 32 * c), st32);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S->tempty[a]));
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (CL > 1) {
-    cluster_sync();
-    // After an error (a wait that gave up), a peer's copy or commit may still
-    // be in flight towards this CTA: give it time to land before either exits.
-    if (threadIdx.x == 0 && read_status(status) != 0) {
-      const uint64_t t0 = globaltimer();
-      while (globaltimer() - t0 < 100000ull) {
-      }
-    }
-    cluster_sync();
-  }
-  tc_fence_after();
-  if (warp == 1)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
-                 : "memory");
-}
-
 // ---------------------------------------------------------------------------
-// CTA-pair kernel (cta_group::2). Clusters of two CTAs, as in k_gemm<2>: CTA
-// r of the pair takes tile 2p + r of a pair of adjacent tiles of one group.
+// CTA-pair kernel (cta_group::2). Clusters of two CTAs: CTA r of the pair
+// takes tile 2p + r of a pair of adjacent tiles of one group.
 // Each CTA stages its own 128x64 x tile and its half (128 columns) of the
 // 256-column weight tile, so a stage is 32 KB per CTA and the ring is 6
 // deep. Both CTAs' copies count on CTA 0's `full` barrier; one thread of CTA
@@ -830,6 +579,20 @@ bool make_map(CUtensorMap* m, const void* ptr, unsigned long long rows, unsigned
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// True when p is device (or managed) memory of the current device: the
+// tensor maps are encoded over these pointers and the kernel's copies read
+// and write through them, so memory of another GPU is refused on the host.
+bool on_current_device(const void* p) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // the lookup failed: clear its (non-sticky) error
+    return false;
+  }
+  return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
+}
+
 // Each group adds at most one partial tile and one padding tile.
 long long max_tiles(int R, int S, int K, int E, int B) {
   return ((long long)R * S * K + kBM - 1) / kBM + 2LL * R * (E + B);
@@ -913,6 +676,9 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
   if (!aligned16(x) || !aligned16(w_home) || !aligned16(y) || !aligned16(ws) ||
       (B > 0 && !aligned16(w_slot)))
     return MEP_ERR_INVALID_ARG;
+  if (!on_current_device(x) || !on_current_device(w_home) || !on_current_device(y) ||
+      (B > 0 && !on_current_device(w_slot)))
+    return MEP_ERR_INVALID_ARG;
   CUtensorMap mx, mh, msl;
   if (!make_map(&mx, x, (unsigned long long)rows, (unsigned long long)H, kBM) ||
       !make_map(&mh, w_home, (unsigned long long)E * H, (unsigned long long)Hp, kBK))
@@ -926,26 +692,17 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
   int* count = static_cast<int*>(ws);
   int4* tiles = reinterpret_cast<int4*>(static_cast<char*>(ws) + 16);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  constexpr int CL = MEP_GEMM_CLUSTER;
   cudaError_t err = launch_pdl(k_gemm_tiles, dim3(1), dim3(kTileThreads), 0, st, cu_seqlens, R,
-                               E, B, int(SK), CL, status, tiles, count);
+                               E, B, int(SK), kPair, status, tiles, count);
   if (err != cudaSuccess) return MEP_ERR_CUDA;
   __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(y);
   const int st32 =
       MEP_GEMM_ST32 && Hp % 16 == 0 && (reinterpret_cast<uintptr_t>(y) & 31u) == 0 ? 1 : 0;
-  if (CL == 2 && MEP_GEMM_PAIR_MMA) {
-    static GridCache cache;
-    if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm_pair), kSmemPair))
-      return MEP_ERR_CUDA;
-    err = launch_gemm(k_gemm_pair, 2, kSmemPair, cache, st, mx, mh, msl, tiles, count, status, E,
-                      H, Hp, yb, st32);
-  } else {
-    static GridCache cache;
-    if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm<CL>), kSmemBytes))
-      return MEP_ERR_CUDA;
-    err = launch_gemm(k_gemm<CL>, CL, kSmemBytes, cache, st, mx, mh, msl, tiles, count, status, E,
-                      H, Hp, yb, st32);
-  }
+  static GridCache cache;
+  if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm_pair), kSmemPair))
+    return MEP_ERR_CUDA;
+  err = launch_gemm(k_gemm_pair, kPair, kSmemPair, cache, st, mx, mh, msl, tiles, count, status, E,
+                    H, Hp, yb, st32);
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
 
