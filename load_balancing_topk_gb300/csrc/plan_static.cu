@@ -13,8 +13,13 @@
 // library is loaded holds MEP_PLAN_STATIC_SCRATCH_BYTES of it until the
 // process exits. In host code its name is only a host-side stand-in for the
 // symbol, never a device address: the device address is looked up with
-// cudaGetSymbolAddress, once per device, on the first call made while that
-// device is current, and cached.
+// cudaGetSymbolAddress on the first call made while a device is current, and
+// cached per device together with the unique id of the CUDA context it was
+// looked up in. A later call in another context (after cudaDeviceReset, or
+// once the primary context has been destroyed and created again, which
+// reloads the module) looks the address up again instead of using a stale one.
+
+#include <cuda.h>
 
 #include <mutex>
 
@@ -26,17 +31,49 @@ __device__ __align__(256) unsigned char g_plan_scratch[MEP_PLAN_STATIC_SCRATCH_B
 
 constexpr int kMaxDevices = 64;
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+// Unique id of the current CUDA context (0 when no context is current yet,
+// or on error).
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 // Device address of g_plan_scratch on the current device (nullptr on error).
 void* plan_scratch_on_current_device() {
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (ctx == 0 || addr[dev] == nullptr || ctx_of[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess) return nullptr;
+    // the lookup makes the device's primary context current if none was
+    if (ctx == 0) ctx = current_context_id();
+    if (ctx == 0) return nullptr;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   return addr[dev];
 }

@@ -3,11 +3,14 @@
 Such callers (a host program that reaches the GPU only through the C ABI,
 or a runtime whose device memory belongs to one pool allocator) cannot hand
 mep_plan a workspace, so this entry point uses a fixed scratch array
-compiled into the library. The test calls it through the C ABI twice in a
-row, on different routings, and checks every output against mep_plan's
-(integer outputs: bit-exact, the tolerance of the plan tests). It also
-checks that sizes needing more scratch than the array holds are refused
-before anything runs.
+compiled into the library. The tests call it through the C ABI several times
+in a row on the shared array, on routings of different sizes in both orders
+(the larger stress routing before and after the medium one, then a small
+routing after the largest), and check every output bit for bit against the
+CPU oracle's plan and against mep_plan's (integer outputs: bit-exact, the
+tolerance of the plan tests). A later, smaller call therefore cannot pass
+on scratch bytes left over from a larger one. They also check that sizes
+needing more scratch than the array holds are refused before anything runs.
 """
 
 import ctypes
@@ -17,6 +20,7 @@ import pytest
 import torch
 
 import load_balancing_topk_gb300 as mep
+import oracle
 from load_balancing_topk_gb300 import _build, synth
 
 pytestmark = pytest.mark.gpu
@@ -46,23 +50,43 @@ def _plan_static(lib, idx_d, s):
     return out
 
 
-def test_static_scratch_plan_matches_mep_plan_on_two_calls_in_a_row(lib):
-    cases = [(synth.MEDIUM, dict(alpha=0.075684), 0),
-             (synth.STRESS, dict(alpha=1.2, kind="hot"), 1)]
-    inputs = []
-    for s, kw, seed in cases:
+CASES = {
+    "medium": (synth.MEDIUM, dict(alpha=0.075684), 0),
+    "stress": (synth.STRESS, dict(alpha=1.2, kind="hot"), 1),
+    "small": (synth.Shape(R=4, E=12, K=3, S=1000, H=8, B=9), dict(alpha=1.0), 2),
+}
+
+
+def _inputs(names):
+    out = []
+    for name in names:
+        s, kw, seed = CASES[name]
         idx, _ = synth.routing(s, seed=seed, **kw)
-        inputs.append((s, torch.from_numpy(idx).to(DEV)))
-    # two calls in a row on the shared scratch, then the workspace entry point
-    static = [_plan_static(lib, idx_d, s) for s, idx_d in inputs]
+        out.append((name, s, idx, torch.from_numpy(idx).to(DEV)))
+    return out
+
+
+@pytest.mark.parametrize("order", [("medium", "stress", "small"), ("stress", "medium", "small")],
+                         ids=lambda o: "-".join(o))
+def test_static_scratch_plan_matches_oracle_and_mep_plan_on_calls_in_a_row(lib, order):
+    inputs = _inputs(order)
+    # calls in a row on the shared scratch, then the workspace entry point
+    static = [_plan_static(lib, idx_d, s) for _, s, _, idx_d in inputs]
     torch.cuda.synchronize()
     static = [{k: v.cpu().numpy() for k, v in o.items()} for o in static]
-    for (s, idx_d), got in zip(inputs, static):
+    for (name, s, idx, idx_d), got in zip(inputs, static):
+        want = oracle.plan(idx, s.R, s.S, s.K, s.E, s.B)
+        assert want["status"] == "ok"
+        assert int(got["status"][0]) == 0, name
+        np.testing.assert_array_equal(got["expert_counts"], want["counts"], err_msg=name)
+        for key in ("cu_seqlens", "slot_expert", "dst_pos"):
+            np.testing.assert_array_equal(got[key], want[key], err_msg=f"{name} {key}")
         ref = mep.mep_plan(idx_d, s.R, s.S, s.K, s.E, s.B)
         torch.cuda.synchronize()
-        assert int(got["status"][0]) == int(ref.status.item()) == 0
-        for name in ("expert_counts", "cu_seqlens", "slot_expert", "dst_pos"):
-            np.testing.assert_array_equal(got[name], getattr(ref, name).cpu().numpy(), err_msg=name)
+        assert int(ref.status.item()) == 0
+        for key in ("expert_counts", "cu_seqlens", "slot_expert", "dst_pos"):
+            np.testing.assert_array_equal(got[key], getattr(ref, key).cpu().numpy(),
+                                          err_msg=f"{name} {key}")
 
 
 def test_static_scratch_refuses_sizes_beyond_its_array(lib):
