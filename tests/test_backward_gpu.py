@@ -52,6 +52,7 @@ SHAPES = [
     synth.Shape(R=2, E=80, K=40, S=50, H=32, B=40),
     synth.Shape(R=2, E=8, K=4, S=96, H=4096, B=4),   # 32-byte vectors in combine_backward
     synth.Shape(R=4, E=128, K=64, S=24, H=40, B=16),  # K = 64, the limit
+    synth.Shape(R=2, E=16, K=8, S=128, H=7168, B=8),  # K = 8 at H = 7168 (32-byte vectors)
 ]
 
 

@@ -57,11 +57,16 @@ def test_random_layer_chain(seed):
     # dispatch / combine
     hidden = synth.bf16_normal(s.N, H, seed=seed, tag=90)
     buf = mep.mep_dispatch(to_dev(hidden), p.dst_pos, p.status, R, S, K)
-    out = mep.mep_combine(buf, to_dev(w), p.dst_pos, p.status, R, S, K)
     torch.cuda.synchronize()
     buf_r = oracle.dispatch(hidden, ref["dst_pos"], s.A)
     np.testing.assert_array_equal(to_np(buf), buf_r)
-    np.testing.assert_array_equal(to_np(out), oracle.combine(buf_r, w, ref["dst_pos"]))
+    # combine of independent expert outputs (a token's K dispatched rows are
+    # equal copies, which would hide a row or weight paired with the wrong k)
+    y_e = synth.bf16_normal(s.A, H, seed=seed, tag=93)
+    buf.copy_(to_dev(y_e))
+    out = mep.mep_combine(buf, to_dev(w), p.dst_pos, p.status, R, S, K)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(out), oracle.combine(y_e, w, ref["dst_pos"]))
 
     # prefetch + grouped GEMM on integer-valued rows and weights
     xi = oracle.f32_to_bf16(synth.integer_valued((s.A, H), seed, -2, 2, tag=91))
