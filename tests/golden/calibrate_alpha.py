@@ -1,6 +1,7 @@
 """Calibrate the synthetic router's Zipf alpha to target maxvio values.
 
-Writes ``zipf_alpha.json`` beside this file. It calls only the seeded input
+Writes ``load_balancing_topk_gb300/zipf_alpha.json``, the table that
+``synth.alpha_for`` reads (inputs, not expected values). It calls only the seeded input
 generator and the CPU oracle (``oracle.counts`` / ``oracle.maxvio``): maxvio
 is max_e T_e / T_bar - 1 ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库",
 section 解决的核心问题). For each workload and target, alpha is bisected at
@@ -55,7 +56,7 @@ def main():
             a, m = calibrate(shape, tgt)
             table[name][f"{tgt:g}"] = round(a, 6)
             print(f"{name} target {tgt:g}: alpha {a:.6f} -> maxvio {m:.4f}", flush=True)
-    out = os.path.join(os.path.dirname(os.path.abspath(__file__)), "zipf_alpha.json")
+    out = os.path.join(ROOT, "load_balancing_topk_gb300", "zipf_alpha.json")
     with open(out, "w") as f:
         json.dump(table, f, indent=1, sort_keys=True)
         f.write("\n")
