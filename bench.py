@@ -1,28 +1,34 @@
 """Benchmark of the dynamic-redundant-expert hot path on GB300.
 
-One step = the whole path over one batch: mep_plan (histogram + planner +
-destination rows) -> mep_dispatch -> mep_combine -> mep_reduce_grad, on the
-E=64 / R=8 / K=6 / S=4096 / H=2048 / B=8 routing workload (Zipf skew tuned
-to maxvio 0.5), with the E=64 / R=8 / B=8 / H=2048 / H'=1408 fp32 gradient
-tensors whose slot map is that step's plan.
+Headline step = one pass of the path over one batch of the R=8 / E=256 /
+K=8 / S=8192 / H=7168 / B=32 workload with the Zipf skew tuned to maxvio
+0.5: mep_plan (histogram + planner + destination rows) -> mep_dispatch ->
+mep_combine. Inputs are resident in HBM and larger than L2 (hidden 0.94 GB,
+buffer 7.5 GB); a 256 MB write still runs before every step, outside the
+timed region. value = the step's algorithmic bytes / its time.
 
 The timed region records CUDA events at the step ends only, so every kernel's
 programmatic dependent launch overlaps its predecessor as in use; a second run
 of the same steps with an event between every two kernels gives the per-kernel
-breakdown and the roofline kernel's duration; a third run replays the same
-step from one captured CUDA graph.
+times and the roofline kernel's launch duration; a third run replays the same
+step from one captured CUDA graph. e2e: the same step through the public API
+with pinned host buffers, host<->device copies inside the timed region.
 
-Printed (one JSON line, rank 0): whole-step GB/s of algorithmic bytes, the
-per-step breakdown (plan us, dispatch+combine GB/s, reduce_grad GB/s), the
-roofline of the dominant kernel against the measured HBM copy peak (and the
-nominal 7.9 TB/s), the next rows (prefetch, backward, grouped GEMM), an
-end-to-end figure through the public API with host buffers, the CPU oracle
-on a bounded sample, SM clocks sampled during the timed region, and a
-maxvio sweep of dispatch+combine on the R=8 / E=256 / K=8 / S=8192 /
-H=7168 workload (plus the R=16 / E=384 stress routing).
+Beside it (one JSON line, rank 0):
+* breakdown -- the medium step: R=8 / E=64 / K=6 / S=4096 / H=2048 / B=8
+  (maxvio 0.5) plan -> dispatch -> combine -> mep_reduce_grad on the
+  E=64 / R=8 / B=8 / H=2048 / H'=1408 fp32 gradients whose slot map is that
+  step's plan, timed the same way;
+* sweep -- dispatch+combine GB/s and plan us across maxvio 0 / 0.5 / 1 / 2 / 4
+  on the large workload, plus the R=16 / E=384 stress routings;
+* next_rows -- prefetch, the backward of dispatch and combine, the grouped
+  GEMM consumer and the inference planner, on the medium workload;
+* roofline of the dominant kernel against the measured HBM copy peak (and the
+  nominal 7.9 TB/s), the CPU oracle on a bounded sample, SM clocks sampled
+  during the timed region.
 
 --impl reference times the CPU oracle (the slow reference implementation)
-on a bounded sample of the same step and prints the same line with
+on a bounded sample of the same headline step and prints the same line with
 "impl": "reference".
 
 Multi-GPU (torchrun): every rank runs its own replica on its own GPU; the
@@ -56,6 +62,15 @@ SWEEP_REPS = 10
 
 # ---------------------------------------------------------------------------
 # workload definitions
+def headline_workload(S: int | None = None):
+    """The large workload at maxvio 0.5 (S may be lowered for a profiling run)."""
+    from load_balancing_topk_gb300 import synth
+
+    s = synth.LARGE if S is None else synth.Shape(R=synth.LARGE.R, E=synth.LARGE.E, K=synth.LARGE.K,
+                                                  S=S, H=synth.LARGE.H, B=synth.LARGE.B)
+    return s, synth.alpha_for("large", 0.5)
+
+
 def medium_workload():
     from load_balancing_topk_gb300 import synth
 
@@ -63,19 +78,22 @@ def medium_workload():
     return s, synth.alpha_for("medium", 0.5)
 
 
-def step_bytes(s, HHp, slot_expert: np.ndarray) -> dict:
-    """Algorithmic bytes of each step of the path."""
+def step_bytes(s, HHp=None, slot_expert=None) -> dict:
+    """Algorithmic bytes of each step of the path (reduce_grad only when a
+    gradient size and slot map are given)."""
     N, A, H = s.N, s.A, s.H
     plan = 2 * 4 * A + 4 * A + 4 * (s.E + s.R * (s.E + s.B) + s.R * s.B)
     dispatch = N * H * 2 + A * H * 2 + 4 * A
     combine = A * H * 2 + N * H * 2 + 8 * A
-    se = slot_expert.reshape(-1)
-    used = int((se >= 0).sum())
-    distinct = int(np.unique(se[se >= 0]).size)
-    M = HHp * 4
-    reduce = 2 * (used + distinct) * M + 4 * se.size
-    return dict(plan=plan, dispatch=dispatch, combine=combine, reduce_grad=reduce,
-                used=used, distinct=distinct)
+    out = dict(plan=plan, dispatch=dispatch, combine=combine, reduce_grad=0, used=0, distinct=0)
+    if slot_expert is not None:
+        se = slot_expert.reshape(-1)
+        used = int((se >= 0).sum())
+        distinct = int(np.unique(se[se >= 0]).size)
+        M = HHp * 4
+        out.update(reduce_grad=2 * (used + distinct) * M + 4 * se.size, used=used, distinct=distinct)
+    out["total"] = out["plan"] + out["dispatch"] + out["combine"] + out["reduce_grad"]
+    return out
 
 
 def measured_peak():
@@ -99,13 +117,17 @@ def measured_bf16_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def traffic_record(kernel: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if its source
-    hash still matches the kernel's current source; else None."""
+KERNEL_SOURCE = {"k_dispatch": "permute.cu", "k_combine": "permute.cu",
+                 "k_reduce_grad": "reduce_grad.cu", "k_offsets": "plan.cu", "k_hist": "plan.cu",
+                 "k_plan": "plan.cu"}
+
+
+def traffic_record(kernel: str, workload: str):
+    """Per-launch DRAM bytes (and how they were obtained) from the committed
+    ncu summary, if its source hash still matches the kernel's current
+    source; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = {"k_dispatch": "permute.cu", "k_combine": "permute.cu", "k_reduce_grad": "reduce_grad.cu",
-           "k_offsets": "plan.cu", "k_hist": "plan.cu", "k_plan": "plan.cu"}[kernel]
-    with open(os.path.join(ROOT, "load_balancing_topk_gb300", "csrc", src), "rb") as f:
+    with open(os.path.join(ROOT, "load_balancing_topk_gb300", "csrc", KERNEL_SOURCE[kernel]), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()[:16]
     try:
         with open(path) as f:
@@ -114,9 +136,9 @@ def traffic_record(kernel: str):
                 if not parts or parts[0].startswith("#"):
                     continue
                 kv = dict(p.split("=", 1) for p in parts if "=" in p)
-                if kv.get("kernel") == kernel and kv.get("workload") == "medium":
+                if kv.get("kernel") == kernel and kv.get("workload") == workload:
                     if kv.get("src_sha") == sha:
-                        return int(kv["dram_bytes_per_launch"])
+                        return int(kv["dram_bytes_per_launch"]), kv.get("how", "captured")
                     return None
     except OSError:
         pass
@@ -239,137 +261,145 @@ def graph_replay(steps, body, reset, new_events, dev):
     return [e[0].elapsed_time(e[4]) for e in events]
 
 
-def gpu_arm(args, rank: int, world: int, dist):
+class StepRunner:
+    """Device-resident inputs and outputs of one step of the path and the step
+    itself: mep_plan -> mep_dispatch -> mep_combine (-> mep_reduce_grad when
+    the step carries gradient tensors), all through the public binding."""
+
+    def __init__(self, s, alpha, dev, seed, flush, grads=False):
+        import torch
+
+        import load_balancing_topk_gb300 as mep
+        from load_balancing_topk_gb300 import synth
+
+        self.s, self.dev, self.flush, self.grads = s, dev, flush, grads
+        self.idx, self.w = synth.routing(s, seed=seed, alpha=alpha)
+        self.x_np = synth.hidden(s, seed=seed)
+        self.idx_d = torch.from_numpy(self.idx).to(dev)
+        self.w_d = torch.from_numpy(self.w).to(dev)
+        self.x_d = torch.from_numpy(self.x_np.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.plan = mep.mep_plan(self.idx_d, s.R, s.S, s.K, s.E, s.B)
+        self.buf = torch.empty((s.A, s.H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((s.N, s.H), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        st = int(self.plan.status.item())
+        assert st == 0, mep.STATUS.get(st)
+        se = self.plan.slot_expert.cpu().numpy()
+        counts = self.plan.expert_counts.cpu().numpy()
+        self.maxvio = float(counts.max() / (s.A / s.E) - 1.0)
+        self.slots_used = int((se >= 0).sum())
+        self.HHp = None
+        if grads:
+            self.HHp = synth.GRAD_H * synth.GRAD_HP
+            home, slots = synth.grads(synth.GRAD_E, synth.GRAD_R, synth.GRAD_B, self.HHp, seed=seed)
+            self.home_d = torch.from_numpy(home).to(dev)
+            self.slots0 = torch.from_numpy(slots).to(dev)
+            self.slots_d = self.slots0.clone()
+            self.used_rows = torch.from_numpy(np.nonzero(se.reshape(-1) >= 0)[0]).to(dev)
+        self.nb = step_bytes(s, self.HHp, se if grads else None)
+        self.launches = mep.plan_kernel_count(s.R, s.S, s.K, s.E, s.B) + 2 + (1 if grads else 0)
+
+    def body(self, ev=None, idx=None, w=None, x=None, out=None):
+        """One step on the current stream; ev[1..3] are recorded between the
+        kernels when given (ev[0] and ev[4] are the caller's)."""
+        import load_balancing_topk_gb300 as mep
+
+        s = self.s
+        idx = self.idx_d if idx is None else idx
+        w = self.w_d if w is None else w
+        x = self.x_d if x is None else x
+        out = self.out if out is None else out
+        p = mep.mep_plan(idx, s.R, s.S, s.K, s.E, s.B, out=self.plan)
+        if ev is not None:
+            ev[1].record()
+        mep.mep_dispatch(x, p.dst_pos, p.status, s.R, s.S, s.K, buf=self.buf)
+        if ev is not None:
+            ev[2].record()
+        mep.mep_combine(self.buf, w, p.dst_pos, p.status, s.R, s.S, s.K, out=out)
+        if ev is not None:
+            ev[3].record()
+        if self.grads:
+            mep.mep_reduce_grad(p.slot_expert, self.home_d, self.slots_d, p.status, s.E)
+
+    def reset(self):
+        """Untimed, between steps: restore the consumed slot gradients, then
+        evict L2 with a > L2 write."""
+        if self.grads:
+            self.slots_d.index_copy_(0, self.used_rows, self.slots0.index_select(0, self.used_rows))
+        self.flush.fill_(float(np.random.rand()))
+
+
+def _events(n=5):
     import torch
 
-    import load_balancing_topk_gb300 as mep
-    from load_balancing_topk_gb300 import synth
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
-    mep.load_library()
-    s, alpha = medium_workload()
-    seed = rank
-    idx, w = synth.routing(s, seed=seed, alpha=alpha)
-    x_np = synth.hidden(s, seed=seed)
-    HHp = synth.GRAD_H * synth.GRAD_HP
-    home_np, slots_np = synth.grads(synth.GRAD_E, synth.GRAD_R, synth.GRAD_B, HHp, seed=seed)
 
-    idx_d = torch.from_numpy(idx).to(dev)
-    w_d = torch.from_numpy(w).to(dev)
-    x_d = torch.from_numpy(x_np.view(np.int16)).to(dev).view(torch.bfloat16)
-    home_d = torch.from_numpy(home_np).to(dev)
-    slots0 = torch.from_numpy(slots_np).to(dev)
-    slots_d = slots0.clone()
-    plan = mep.mep_plan(idx_d, s.R, s.S, s.K, s.E, s.B)
-    buf = torch.empty((s.A, s.H), dtype=torch.bfloat16, device=dev)
-    out = torch.empty((s.N, s.H), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    torch.cuda.synchronize()
-    assert int(plan.status.item()) == 0, mep.STATUS.get(int(plan.status.item()))
-    se = plan.slot_expert.cpu().numpy()
-    counts = plan.expert_counts.cpu().numpy()
-    maxvio = float(counts.max() / (s.A / s.E) - 1.0)
-    nb = step_bytes(s, HHp, se)
-    used_rows = torch.from_numpy(np.nonzero(se.reshape(-1) >= 0)[0]).to(dev)
+def time_steps(runner, args, dist):
+    """Warm-up, then the timed region (K steps, events at the step ends only),
+    then the same K steps with an event between every two kernels, then K
+    replays of the step captured in a CUDA graph. Returns per-step times (ms)
+    and the wall-clock span of the first two runs."""
+    import torch
 
-    def step(e, per_kernel):
-        # per_kernel=False: events only at the step's ends, so each kernel's
-        # programmatic dependent launch overlaps its predecessor's tail as it
-        # does in use; an event between two kernels would hold the second
-        # back until the first has drained.
-        e[0].record()
-        mep.mep_plan(idx_d, s.R, s.S, s.K, s.E, s.B, out=plan)
-        if per_kernel:
-            e[1].record()
-        mep.mep_dispatch(x_d, plan.dst_pos, plan.status, s.R, s.S, s.K, buf=buf)
-        if per_kernel:
-            e[2].record()
-        mep.mep_combine(buf, w_d, plan.dst_pos, plan.status, s.R, s.S, s.K, out=out)
-        if per_kernel:
-            e[3].record()
-        mep.mep_reduce_grad(plan.slot_expert, home_d, slots_d, plan.status, s.E)
-        e[4].record()
-
-    def step_body():
-        mep.mep_plan(idx_d, s.R, s.S, s.K, s.E, s.B, out=plan)
-        mep.mep_dispatch(x_d, plan.dst_pos, plan.status, s.R, s.S, s.K, buf=buf)
-        mep.mep_combine(buf, w_d, plan.dst_pos, plan.status, s.R, s.S, s.K, out=out)
-        mep.mep_reduce_grad(plan.slot_expert, home_d, slots_d, plan.status, s.E)
-
-    def untimed_reset():
-        # restore the consumed slot gradients, then evict L2 with a > L2 write
-        slots_d.index_copy_(0, used_rows, slots0.index_select(0, used_rows))
-        flush.fill_(float(np.random.rand()))
-
-    def new_events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-
-    for _ in range(args.warmup):
-        untimed_reset()
-        step(new_events(), True)
-    torch.cuda.synchronize()
-
-    sampler = ClockSampler(dev.index).start()
-    time.sleep(0.3)
     times = {"step": [], "plan": [], "dispatch": [], "combine": [], "reduce_grad": [],
              "step_per_kernel_events": []}
+
+    def one(per_kernel):
+        runner.reset()
+        e = _events()
+        e[0].record()
+        runner.body(e if per_kernel else None)
+        e[4].record()
+        return e
+
+    for _ in range(args.warmup):
+        one(True)
+    torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    # the timed region: K steps, events at the step ends only
-    events = []
-    for _ in range(args.steps):
-        untimed_reset()
-        e = new_events()
-        step(e, False)
-        events.append(e)
+    ev = [one(False) for _ in range(args.steps)]
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    for e in events:
-        times["step"].append(e[0].elapsed_time(e[4]))
-    total_ms = sum(times["step"])
-    # the same K steps again with an event between every two kernels: the
-    # per-kernel breakdown and the roofline kernel's launch duration
-    events = []
-    for _ in range(args.steps):
-        untimed_reset()
-        e = new_events()
-        step(e, True)
-        events.append(e)
+    times["step"] = [e[0].elapsed_time(e[4]) for e in ev]
+    ev = [one(True) for _ in range(args.steps)]
     torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
     t_wall1 = time.time()
-    for e in events:
+    for e in ev:
         times["plan"].append(e[0].elapsed_time(e[1]))
         times["dispatch"].append(e[1].elapsed_time(e[2]))
         times["combine"].append(e[2].elapsed_time(e[3]))
         times["reduce_grad"].append(e[3].elapsed_time(e[4]))
         times["step_per_kernel_events"].append(e[0].elapsed_time(e[4]))
-    assert int(plan.status.item()) == 0
-    times["graph_step"] = graph_replay(args.steps, step_body, untimed_reset, new_events, dev)
-    assert int(plan.status.item()) == 0
+    assert int(runner.plan.status.item()) == 0
+    times["graph_step"] = graph_replay(args.steps, runner.body, runner.reset, _events, runner.dev)
+    assert int(runner.plan.status.item()) == 0
+    return times, (t_wall0, t_wall1)
 
-    nxt = next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp) if rank == 0 else None
 
-    # --- end to end through the public API with host buffers -------------
-    # Every step copies its inputs (topk_idx, topk_w, hidden) from pinned host
-    # memory and its result (out, status) back, inside the timed region. The
-    # copies run on their own streams, double-buffered, so step i+1's inputs
-    # and step i-1's result move while step i computes.
-    idx_h = torch.from_numpy(idx).pin_memory()
-    w_h = torch.from_numpy(w).pin_memory()
-    x_h = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
-    sets = [dict(idx=torch.empty_like(idx_d), w=torch.empty_like(w_d), x=torch.empty_like(x_d),
-                 out=torch.empty_like(out),
+def end_to_end(runner, args):
+    """The step through the public API with host buffers: every step copies
+    its inputs (topk_idx, topk_w, hidden) from pinned host memory and its
+    result (out, status) back, inside the timed region. The copies run on
+    their own streams, double-buffered, so step i+1's inputs and step i-1's
+    result move while step i computes. Also times the same copies alone (the
+    host-link bound). Returns (ms per step, h2d bytes, d2h bytes, link ms)."""
+    import torch
+
+    s = runner.s
+    idx_h = torch.from_numpy(runner.idx).pin_memory()
+    w_h = torch.from_numpy(runner.w).pin_memory()
+    x_h = torch.from_numpy(runner.x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    sets = [dict(idx=torch.empty_like(runner.idx_d), w=torch.empty_like(runner.w_d),
+                 x=torch.empty_like(runner.x_d), out=torch.empty_like(runner.out),
                  out_h=torch.empty((s.N, s.H), dtype=torch.bfloat16).pin_memory(),
                  st_h=torch.empty(1, dtype=torch.int32).pin_memory()) for _ in range(2)]
     s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_run(nsteps):
+    def run(nsteps):
         ev = [[torch.cuda.Event() for _ in range(3)] for _ in range(nsteps)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
@@ -387,11 +417,8 @@ def gpu_arm(args, rank: int, world: int, dist):
             if i >= 2:
                 s_cmp.wait_event(ev[i - 2][2])      # step i-2's result has left this out buffer
             with torch.cuda.stream(s_cmp):
-                p2 = mep.mep_plan(b["idx"], s.R, s.S, s.K, s.E, s.B, out=plan)
-                mep.mep_dispatch(b["x"], p2.dst_pos, p2.status, s.R, s.S, s.K, buf=buf)
-                mep.mep_combine(buf, b["w"], p2.dst_pos, p2.status, s.R, s.S, s.K, out=b["out"])
-                mep.mep_reduce_grad(p2.slot_expert, home_d, slots_d, p2.status, s.E)
-                b["st_h"].copy_(p2.status, non_blocking=True)
+                runner.body(idx=b["idx"], w=b["w"], x=b["x"], out=b["out"])
+                b["st_h"].copy_(runner.plan.status, non_blocking=True)
                 ev[i][1].record(s_cmp)
             s_out.wait_event(ev[i][1])
             with torch.cuda.stream(s_out):
@@ -401,16 +428,15 @@ def gpu_arm(args, rank: int, world: int, dist):
         t1.synchronize()
         return t0.elapsed_time(t1)
 
-    e2e_run(max(3, args.warmup))
-    e2e_steps = max(3, min(args.steps, 200))
-    e2e_ms = [e2e_run(e2e_steps) / e2e_steps]
+    run(max(3, args.warmup))
+    nsteps = max(3, min(args.steps, 200))
+    ms = run(nsteps) / nsteps
     assert all(int(b["st_h"].item()) == 0 for b in sets)
-    h2d = idx.nbytes + w.nbytes + x_np.nbytes
+    h2d = runner.idx.nbytes + runner.w.nbytes + runner.x_np.nbytes
     d2h = s.N * s.H * 2 + 4
 
     def copies_only(reps=5):
-        """The same per-step copies, both directions at once, no compute:
-        the host-link bound of the end-to-end step."""
+        """The same per-step copies, both directions at once, no compute."""
         b = sets[0]
         ts = []
         for r in range(reps + 1):
@@ -425,7 +451,7 @@ def gpu_arm(args, rank: int, world: int, dist):
                 e_in.record(s_in)
             with torch.cuda.stream(s_out):
                 b["out_h"].copy_(b["out"], non_blocking=True)
-                b["st_h"].copy_(plan.status, non_blocking=True)
+                b["st_h"].copy_(runner.plan.status, non_blocking=True)
                 e_out.record(s_out)
             torch.cuda.synchronize()
             if r:
@@ -433,30 +459,88 @@ def gpu_arm(args, rank: int, world: int, dist):
         return float(np.median(ts))
 
     link_ms = copies_only()
+    del sets
+    torch.cuda.empty_cache()
+    return ms, h2d, d2h, link_ms
 
-    sweep = run_sweep(args, dev, rank) if (args.sweep and rank == 0) else None
+
+def step_summary(runner, times, peak):
+    """Per-kernel breakdown of one runner's timed steps."""
+    nb = runner.nb
+    med = {k: float(np.median(v)) for k, v in times.items() if v}
+    avg = {k: float(np.mean(v)) for k, v in times.items() if v}
+    dc_ms = avg["dispatch"] + avg["combine"]
+    dc_gbs = (nb["dispatch"] + nb["combine"]) / (dc_ms / 1e3) / 1e9
+    out = {
+        "plan_us": round(1000 * med["plan"], 2),
+        "dispatch_ms": round(med["dispatch"], 4), "combine_ms": round(med["combine"], 4),
+        "dispatch_gbs": round(nb["dispatch"] / (avg["dispatch"] / 1e3) / 1e9, 1),
+        "combine_gbs": round(nb["combine"] / (avg["combine"] / 1e3) / 1e9, 1),
+        "dispatch_combine_gbs": round(dc_gbs, 1),
+        "dispatch_combine_frac_of_peak": round(dc_gbs / peak, 4),
+        "dispatch_combine_frac_of_nominal": round(dc_gbs / NOMINAL_HBM_GBS, 4),
+        "tokens_per_s": round(runner.s.N / (dc_ms / 1e3), 0),
+        "step_bytes": nb["total"],
+        "step_ms_with_per_kernel_events": round(med["step_per_kernel_events"], 4),
+        "graph_replay_ms_per_step": round(avg["graph_step"], 4),
+        "slots_used": runner.slots_used,
+    }
+    if runner.grads:
+        rg = nb["reduce_grad"] / (avg["reduce_grad"] / 1e3) / 1e9
+        out.update(reduce_grad_ms=round(med["reduce_grad"], 4), reduce_grad_gbs=round(rg, 1),
+                   reduce_grad_frac_of_peak=round(rg / peak, 4),
+                   reduce_grad_frac_of_nominal=round(rg / NOMINAL_HBM_GBS, 4),
+                   reduce_grad_slots_used=nb["used"], reduce_grad_experts=nb["distinct"])
+    return out, avg
+
+
+def gpu_arm(args, rank: int, world: int, dist):
+    import torch
+
+    import load_balancing_topk_gb300 as mep
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    mep.load_library()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    seed = rank
+    s, alpha = headline_workload(args.tokens_per_rank)
+    main_r = StepRunner(s, alpha, dev, seed, flush)
+    med_r = None
+    if args.medium:
+        sm, alpha_m = medium_workload()
+        med_r = StepRunner(sm, alpha_m, dev, seed, flush, grads=True)
+
+    sampler = ClockSampler(dev.index).start()
+    time.sleep(0.3)
+    times, t_wall = time_steps(main_r, args, dist)
+    e2e = end_to_end(main_r, args) if args.e2e else None
+    med_times = time_steps(med_r, args, dist)[0] if med_r is not None else None
+    nxt = next_rows(args, med_r) if (rank == 0 and med_r is not None and args.next_rows) else None
+    sweep = run_sweep(args, main_r, rank) if (args.sweep and rank == 0) else None
     sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
+    clocks = sampler.summary(*t_wall)
 
-    total_bytes = nb["plan"] + nb["dispatch"] + nb["combine"] + nb["reduce_grad"]
-    t_max, e2e_max = max_over_ranks([total_ms, float(np.median(e2e_ms))], dist, dev)
-    res = dict(
-        next_rows=nxt,
-        total_ms=t_max, steps=args.steps, total_bytes=total_bytes, nb=nb, times=times,
-        maxvio=maxvio, e2e_ms=e2e_max, h2d=h2d, d2h=d2h, link_ms=link_ms, clocks=clocks, sweep=sweep,
-        t_wall=(t_wall0, t_wall1), shape=s, HHp=HHp,
-    )
-    return res
+    total_ms = sum(times["step"])
+    vals = [total_ms, e2e[0] if e2e else 0.0]
+    t_max, e2e_max = max_over_ranks(vals, dist, dev)
+    return dict(main=main_r, times=times, total_ms=t_max, e2e=e2e, e2e_ms=e2e_max, medium=med_r,
+                med_times=med_times, next_rows=nxt, sweep=sweep, clocks=clocks)
 
 
-def next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp):
-    """Throughput of the steps beyond the forward/backward hot path on the
-    same workload: replica weight prefetch (bf16 E x H x H' weights, the
-    step's slot map) and the backward of dispatch and combine."""
+def next_rows(args, runner):
+    """Throughput of the rows beyond the hot path on the medium workload:
+    replica weight prefetch (bf16 E x H x H' weights, the step's slot map),
+    reduce_grad with every slot in use, the backward of dispatch and combine,
+    the grouped GEMM consumer and the inference planner."""
     import torch
 
     import load_balancing_topk_gb300 as mep
     from load_balancing_topk_gb300 import synth
+
+    s, dev, idx_d, w_d = runner.s, runner.dev, runner.idx_d, runner.w_d
+    # the plan, buffer and output of the step's last timed pass
+    plan, buf, out, flush, HHp = runner.plan, runner.buf, runner.out, runner.flush, runner.HHp
 
     peak, _ = measured_peak()
     reps = 20
@@ -553,22 +637,21 @@ def next_rows(args, s, dev, idx_d, w_d, x_d, plan, buf, out, flush, HHp):
     return res
 
 
-def run_sweep(args, dev, rank):
+def run_sweep(args, runner, rank):
     """dispatch+combine GB/s across maxvio on the large workload, plus the
-    stress routing; plan latency per point."""
+    stress routings; plan latency per point. Reuses the headline step's
+    hidden rows, buffer and output (the same [65536, 7168] / [524288, 7168]
+    shapes at every point)."""
     peak, _ = measured_peak()
     import torch
 
     import load_balancing_topk_gb300 as mep
     from load_balancing_topk_gb300 import synth
 
-    g = torch.Generator(device=dev)
-    g.manual_seed(1234 + rank)
     big = synth.LARGE
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    x = torch.randn((big.N, big.H), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-    buf = torch.empty((big.A, big.H), dtype=torch.bfloat16, device=dev)
-    out = torch.empty((big.N, big.H), dtype=torch.bfloat16, device=dev)
+    dev, flush, x, buf, out = runner.dev, runner.flush, runner.x_d, runner.buf, runner.out
+    if runner.s != big:
+        return None
     points = [("large", 0.0, dict(kind="round_robin"))]
     for m in (0.5, 1.0, 2.0, 4.0):
         points.append(("large", m, dict(alpha=synth.alpha_for("large", m))))
@@ -622,30 +705,29 @@ def run_sweep(args, dev, rank):
                          frac_of_nominal=round(nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 4)))
     gbs = [r["dispatch_combine_gbs"] for r in rows if r.get("workload") == "large" and "dispatch_combine_gbs" in r]
     flat = round(max(gbs) / min(gbs), 4) if gbs else None
-    del x, buf, out, flush
-    torch.cuda.empty_cache()
     return dict(points=rows, flatness_max_over_min_large=flat,
                 note="inputs > L2 (hidden 0.94 GB, buffer 7.5 GB), L2 flushed before each rep; "
-                     "median of 10 reps after 3 warm-up")
+                     "median of 10 reps after 3 warm-up; dispatch and combine timed back to back "
+                     "(events around each)")
 
 
 # ---------------------------------------------------------------------------
-def oracle_step_sample(frac: float, seed: int = 0, reps: int = 1) -> dict:
+def oracle_step_sample(s, alpha, frac: float, grads: bool, seed: int = 0, reps: int = 1) -> dict:
     """Run the CPU oracle over a bounded sample of one step: the full plan,
-    dispatch and combine of the first frac of the tokens, and reduce_grad
-    over the first frac of every gradient matrix, reps times over the same
-    inputs. Returns bytes and seconds summed over the reps."""
+    dispatch and combine of the first frac of the tokens, and (grads)
+    reduce_grad over the first frac of every gradient matrix, reps times over
+    the same inputs. Returns bytes and seconds summed over the reps."""
     import oracle
     from load_balancing_topk_gb300 import synth
 
-    s, alpha = medium_workload()
     idx, w = synth.routing(s, seed=seed, alpha=alpha)
     n_tok = max(1, int(s.N * frac))
     x = synth.bf16_normal(n_tok, s.H, seed=seed)
     HHp = max(4, int(synth.GRAD_H * synth.GRAD_HP * frac))
-    rng = np.random.default_rng(seed)
-    home = rng.standard_normal((synth.GRAD_E, HHp), dtype=np.float32) * np.float32(1e-3)
-    slots = rng.standard_normal((synth.GRAD_R * synth.GRAD_B, HHp), dtype=np.float32) * np.float32(1e-3)
+    if grads:
+        rng = np.random.default_rng(seed)
+        home = rng.standard_normal((synth.GRAD_E, HHp), dtype=np.float32) * np.float32(1e-3)
+        slots = rng.standard_normal((synth.GRAD_R * synth.GRAD_B, HHp), dtype=np.float32) * np.float32(1e-3)
     tp = td = tc = tr = 0.0
     for _ in range(reps):
         t0 = time.perf_counter()
@@ -662,92 +744,101 @@ def oracle_step_sample(frac: float, seed: int = 0, reps: int = 1) -> dict:
         t2 = time.perf_counter()
         out = oracle.combine(buf, w[:n_tok], dense)
         t3 = time.perf_counter()
-        st, h2, s2 = oracle.reduce_grad(p["slot_expert"], home, slots, synth.GRAD_E)
+        if grads:
+            st, h2, s2 = oracle.reduce_grad(p["slot_expert"], home, slots, synth.GRAD_E)
+            assert st == "ok"
         t4 = time.perf_counter()
         tp, td, tc, tr = tp + t1 - t0, td + t2 - t1, tc + t3 - t2, tr + t4 - t3
-    nb = step_bytes(synth.Shape(R=s.R, E=s.E, K=s.K, S=max(1, n_tok // s.R), H=s.H, B=s.B),
-                    HHp, p["slot_expert"])
-    nb["plan"] = step_bytes(s, HHp, p["slot_expert"])["plan"]
+    sub = synth.Shape(R=s.R, E=s.E, K=s.K, S=max(1, n_tok // s.R), H=s.H, B=s.B)
+    nb = step_bytes(sub, HHp if grads else None, p["slot_expert"] if grads else None)
+    nb["plan"] = step_bytes(s)["plan"]
     total = nb["plan"] + nb["dispatch"] + nb["combine"] + nb["reduce_grad"]
-    assert out.shape[0] == n_tok and st == "ok"
+    assert out.shape[0] == n_tok and p["status"] == "ok"
     maxvio = float(np.max(p["counts"]) / (s.A / s.E) - 1.0)
     return dict(bytes=total * reps, seconds=tp + td + tc + tr, plan_s=tp, dispatch_s=td,
                 combine_s=tc, reduce_s=tr, frac=frac, n_tok=n_tok, reps=reps, maxvio=maxvio)
 
 
-def cpu_baseline(budget_s: float = 12.0) -> dict:
+def _host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def _sample_text(r, s, frac, grads, seconds):
+    g = f"; reduce_grad on {frac:.4f} of each gradient matrix" if grads else ""
+    return (f"{r['reps']} step(s), each: full plan of {s.N} tokens, dispatch/combine of {r['n_tok']} "
+            f"of them{g}; single-threaded C oracle, {seconds:.1f} s")
+
+
+def cpu_baseline(s, alpha, grads, budget_s: float = 12.0) -> dict:
     """The oracle timed on about budget_s of CPU work: a token fraction of one
     step while one step would take longer, else whole steps repeated."""
-    probe = oracle_step_sample(0.02)
-    frac = min(1.0, 0.02 * budget_s / max(probe["seconds"], 1e-3) / 2.0)
-    r = oracle_step_sample(frac)
+    probe = oracle_step_sample(s, alpha, 0.01, grads)
+    frac = min(1.0, 0.01 * budget_s / max(probe["seconds"], 1e-3) / 2.0)
+    r = oracle_step_sample(s, alpha, frac, grads)
     if frac == 1.0 and r["seconds"] < budget_s:
         reps = max(1, int(round((budget_s - r["seconds"]) / max(r["seconds"], 1e-3))))
-        more = oracle_step_sample(1.0, reps=reps)
+        more = oracle_step_sample(s, alpha, 1.0, grads, reps=reps)
         r = dict(more, bytes=more["bytes"] + r["bytes"], seconds=more["seconds"] + r["seconds"],
                  reps=reps + 1)
     return {"value": round(r["bytes"] / r["seconds"] / 1e9, 3), "unit": "GB/s", "cores": 1,
-            "host_cores": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
-            else os.cpu_count(),
-            "kind": "oracle",
-            "sample": (f"{r['reps']} step(s) on {r['n_tok']} of 32768 tokens each (full plan; "
-                       f"dispatch/combine of those tokens; reduce_grad on {frac:.3f} of each "
-                       f"gradient matrix), single-threaded C, {r['seconds']:.1f} s")}
+            "host_cores": _host_cores(), "kind": "oracle",
+            "sample": _sample_text(r, s, frac, grads, r["seconds"])}
 
 
 def reference_arm(args):
-    """The CPU oracle as the reference implementation, on a bounded sample."""
+    """The CPU oracle as the reference implementation, on a bounded sample of
+    the headline step."""
     budget = 90.0
-    probe = oracle_step_sample(0.01)
+    s, alpha = headline_workload(args.tokens_per_rank)
+    probe = oracle_step_sample(s, alpha, 0.005, False)
     per_step = budget / max(1, args.steps + args.warmup)
-    frac = min(1.0, 0.01 * per_step / max(probe["seconds"], 1e-3))
+    frac = min(1.0, 0.005 * per_step / max(probe["seconds"], 1e-3))
     for _ in range(args.warmup):
-        oracle_step_sample(frac)
+        oracle_step_sample(s, alpha, frac, False)
     tot_b, tot_s = 0, 0.0
     for _ in range(args.steps):
-        r = oracle_step_sample(frac)
+        r = oracle_step_sample(s, alpha, frac, False)
         tot_b += r["bytes"]
         tot_s += r["seconds"]
     value = tot_b / tot_s / 1e9
-    s, _ = medium_workload()
-    sample = (f"each step: full plan + dispatch/combine of {r['n_tok']} of {s.N} tokens + "
-              f"reduce_grad on {frac:.4f} of each gradient matrix; single-threaded C oracle")
+    sample = _sample_text(dict(r, reps=args.steps), s, frac, False, tot_s)
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1000 * tot_s / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(s, r["maxvio"]),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                             "host_cores": len(os.sched_getaffinity(0))
-                             if hasattr(os, "sched_getaffinity") else os.cpu_count(),
-                             "kind": "oracle", "sample": sample},
+                             "host_cores": _host_cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def workload_config(s, maxvio):
-    from load_balancing_topk_gb300 import synth
-
-    return {"workload": (f"moe-layer R{s.R} E{s.E} K{s.K} S{s.S} H{s.H} B{s.B} zipf maxvio~0.5 + "
-                         f"reduce_grad E{synth.GRAD_E} R{synth.GRAD_R} B{synth.GRAD_B} "
-                         f"H{synth.GRAD_H} H'{synth.GRAD_HP}"),
+    return {"workload": (f"moe-layer R{s.R} E{s.E} K{s.K} S{s.S} H{s.H} B{s.B} zipf maxvio~0.5: "
+                         "plan + dispatch + combine"),
             "R": s.R, "E": s.E, "K": s.K, "S": s.S, "H": s.H, "B": s.B,
-            "grad": {"E": synth.GRAD_E, "R": synth.GRAD_R, "B": synth.GRAD_B,
-                     "H": synth.GRAD_H, "Hp": synth.GRAD_HP},
             "maxvio": None if maxvio is None else round(maxvio, 4),
-            "global_batch_tokens": s.N, "l2": "flushed (256 MB write) before every timed step",
-            "arith": "int32 plan; bf16 bit copy; fp32-fma combine -> bf16; fp32 reduce_grad"}
+            "global_batch_tokens": s.N,
+            "l2": "inputs larger than L2 (hidden %.2f GB, buffer %.2f GB); a 256 MB write also runs "
+                  "before every timed step" % (s.N * s.H * 2 / 1e9, s.A * s.H * 2 / 1e9),
+            "arith": "int32 plan; bf16 bit copy; fp32-fma combine -> bf16"}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mep", choices=["mep", "reference"])
+    ap.add_argument("--tokens-per-rank", type=int, default=None,
+                    help="lower S of the headline workload (profiling runs only)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-medium", dest="medium", action="store_false",
+                    help="skip the medium step (and the next rows measured on it)")
+    ap.add_argument("--no-next-rows", dest="next_rows", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -769,25 +860,41 @@ def main():
         tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
         dist = tdist
     res = gpu_arm(args, rank, world, dist)
-    cpu = cpu_baseline() if (args.cpu and rank == 0) else None
+    main_r, med_r = res["main"], res["medium"]
+    cpu = cpu_baseline(main_r.s, headline_workload(args.tokens_per_rank)[1], False) \
+        if (args.cpu and rank == 0) else None
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if rank != 0:
         return
-    s = res["shape"]
-    nb, times = res["nb"], res["times"]
+    s = main_r.s
     K = args.steps
-    ms_step = res["total_ms"] / K
-    value = whole_job_gbs(world, K * res["total_bytes"], res["total_ms"])
-    med = {k: float(np.median(v)) for k, v in times.items()}
-    avg = {k: float(np.mean(v)) for k, v in times.items()}
+    nb = main_r.nb
     peak, peak_kind = measured_peak()
-    # dominant kernel: the larger of dispatch and combine by average time
-    dom = max(("dispatch", "combine", "reduce_grad"), key=lambda k: avg[k])
-    kname = {"dispatch": "k_dispatch", "combine": "k_combine", "reduce_grad": "k_reduce_grad"}[dom]
+    value = whole_job_gbs(world, K * nb["total"], res["total_ms"])
+    summary, avg = step_summary(main_r, res["times"], peak)
+    # the dominant kernel: the larger of dispatch and combine by average time
+    dom = max(("dispatch", "combine"), key=lambda k: avg[k])
+    kname = {"dispatch": "k_dispatch", "combine": "k_combine"}[dom]
     achieved = nb[dom] / (avg[dom] / 1e3) / 1e9
-    dc_gbs = (nb["dispatch"] + nb["combine"]) / ((avg["dispatch"] + avg["combine"]) / 1e3) / 1e9
+    wl = "large" if args.tokens_per_rank is None else None
+    tr = traffic_record(kname, wl) if wl else None
+    summary["note"] = ("per-kernel times from a second run of the same K steps with an event between "
+                       "every two kernels (which holds back each programmatic dependent launch); value "
+                       "and ms_per_step come from the timed steps with events at the step ends only; "
+                       "graph_replay_ms_per_step: the same step captured once in a CUDA graph and "
+                       "replayed K times (mean), with the same untimed reset between replays")
+    if med_r is not None:
+        ms_med = float(np.sum(res["med_times"]["step"])) / K
+        msum, _ = step_summary(med_r, res["med_times"], peak)
+        msum.update(workload=(f"moe-layer R{med_r.s.R} E{med_r.s.E} K{med_r.s.K} S{med_r.s.S} "
+                              f"H{med_r.s.H} B{med_r.s.B} zipf maxvio~0.5 + reduce_grad E64 R8 B8 H2048 "
+                              f"H'1408 on that plan's slot map"),
+                    maxvio=round(med_r.maxvio, 4), ms_per_step=round(ms_med, 4),
+                    gbs=round(med_r.nb["total"] / (ms_med / 1e3) / 1e9, 1),
+                    frac_of_peak=round(med_r.nb["total"] / (ms_med / 1e3) / 1e9 / peak, 4))
+        summary["medium_step"] = msum
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -795,56 +902,41 @@ def main():
         "n_gpus": world,
         "steps": K,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 4),
+        "ms_per_step": round(res["total_ms"] / K, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": workload_config(s, res["maxvio"]),
+        "config": workload_config(s, main_r.maxvio),
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                     "traffic": traffic_record(kname),
-                     "algorithmic_bytes_per_launch": nb[dom]},
-        "breakdown": {
-            "plan_us": round(1000 * med["plan"], 2),
-            "dispatch_ms": round(med["dispatch"], 4), "combine_ms": round(med["combine"], 4),
-            "dispatch_combine_gbs": round(dc_gbs, 1),
-            "dispatch_combine_frac_of_peak": round(dc_gbs / peak, 4),
-            "dispatch_combine_frac_of_nominal": round(dc_gbs / NOMINAL_HBM_GBS, 4),
-            "reduce_grad_ms": round(med["reduce_grad"], 4),
-            "reduce_grad_gbs": round(nb["reduce_grad"] / (avg["reduce_grad"] / 1e3) / 1e9, 1),
-            "reduce_grad_frac_of_nominal": round(
-                nb["reduce_grad"] / (avg["reduce_grad"] / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
-            "reduce_grad_slots_used": nb["used"],
-            "tokens_per_s": round(s.N / ((avg["dispatch"] + avg["combine"]) / 1e3), 0),
-            "step_bytes": res["total_bytes"],
-            "step_ms_with_per_kernel_events": round(med["step_per_kernel_events"], 4),
-            "graph_replay_ms_per_step": round(avg["graph_step"], 4),
-            "note": "per-kernel times from a second run of the same K steps with an event between "
-                    "every two kernels (which holds back each programmatic dependent launch); "
-                    "value and ms_per_step come from the timed steps with events at the step ends only; "
-                    "graph_replay_ms_per_step: the same step captured once in a CUDA graph and "
-                    "replayed K times (mean), with the same untimed reset between replays",
-        },
-        "e2e": {"value": round(whole_job_gbs(world, res["total_bytes"], res["e2e_ms"]), 1),
-                "unit": "GB/s", "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
-                "ms_per_step": round(res["e2e_ms"], 4),
-                "copy_bound": {"ms_per_step": round(res["link_ms"], 4),
-                               "link_gbs": round((res["h2d"] + res["d2h"]) / res["link_ms"] / 1e6, 1),
-                               "frac": round(res["link_ms"] / res["e2e_ms"], 4),
-                               "note": "the same copies alone, both directions at once, no compute"},
-                "note": "every step: pinned host topk_idx/topk_w/hidden -> device, full step, "
-                        "out+status -> host; copies on their own streams, double-buffered, overlapping "
-                        "the neighbouring steps' compute; gradient tensors stay device-resident"},
-        "gpu_launches": 6 * K,
+                     "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+                                     if peak_kind == "measured" else "fallback"),
+                     "traffic": tr[0] if tr else None,
+                     "traffic_source": tr[1] if tr else None,
+                     "algorithmic_bytes_per_launch": nb[dom],
+                     "launch_ms_avg": round(avg[dom], 4)},
+        "breakdown": summary,
+        "gpu_launches": K * main_r.launches,
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
         "sweep": res["sweep"],
         "next_rows": res["next_rows"],
     }
+    if res["e2e"] is not None:
+        e_ms, h2d, d2h, link_ms = res["e2e"]
+        line["e2e"] = {"value": round(whole_job_gbs(world, nb["total"], res["e2e_ms"]), 1),
+                       "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(res["e2e_ms"], 4),
+                       "copy_bound": {"ms_per_step": round(link_ms, 4),
+                                      "link_gbs": round((h2d + d2h) / link_ms / 1e6, 1),
+                                      "frac": round(link_ms / res["e2e_ms"], 4),
+                                      "note": "the same copies alone, both directions at once, no compute"},
+                       "note": "every step: pinned host topk_idx/topk_w/hidden -> device, plan + dispatch "
+                               "+ combine, out+status -> host; copies on their own streams, "
+                               "double-buffered, overlapping the neighbouring steps' compute"}
     print(json.dumps(line), flush=True)
 
 

@@ -90,6 +90,14 @@ MEP_API const char* mep_status_string(int code);
 MEP_API int mep_plan_workspace_bytes(int R, int S, int K, int E, int B, size_t* bytes);
 
 /*
+ * mep_plan_kernel_count -- number of kernels one mep_plan (or
+ * mep_plan_remote_fallback) call enqueues for these sizes. Writes it to
+ * *count. For launch accounting only: nothing is enqueued.
+ * Returns MEP_ERR_INVALID_ARG for sizes mep_plan would reject.
+ */
+MEP_API int mep_plan_kernel_count(int R, int S, int K, int E, int B, int* count);
+
+/*
  * mep_plan -- routing histogram, online planner and destination rows.
  *
  * Problem ("月之暗面开源MoonEP：面向MoE训练的专家并行通信库", 解决的核心问题 and

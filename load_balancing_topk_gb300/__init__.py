@@ -30,7 +30,7 @@ from typing import NamedTuple, Optional
 
 __all__ = [
     "MepError", "Plan", "library_path", "load_library", "status_string", "version",
-    "plan_workspace_bytes", "mep_plan", "mep_plan_remote_fallback", "mep_dispatch", "mep_combine", "mep_reduce_grad",
+    "plan_workspace_bytes", "plan_kernel_count", "mep_plan", "mep_plan_remote_fallback", "mep_dispatch", "mep_combine", "mep_reduce_grad",
     "mep_prefetch", "mep_dispatch_backward", "mep_combine_backward", "STATUS",
 ]
 
@@ -60,6 +60,7 @@ SIGNATURES = [
     ("mep_version", _I, []),
     ("mep_status_string", ctypes.c_char_p, [_I]),
     ("mep_plan_workspace_bytes", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]),
+    ("mep_plan_kernel_count", _I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     ("mep_plan", _I, [_VP, _I, _I, _I, _I, _I, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("mep_plan_remote_fallback", _I, [_VP, _I, _I, _I, _I, _I, _VP, ctypes.c_size_t, _VP, _VP, _VP, _VP, _VP, _VP]),
     ("mep_plan_static_scratch", _I, [_VP, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -126,6 +127,13 @@ def plan_workspace_bytes(R: int, S: int, K: int, E: int, B: int) -> int:
     _check("mep_plan_workspace_bytes",
            load_library().mep_plan_workspace_bytes(R, S, K, E, B, ctypes.byref(out)))
     return int(out.value)
+
+
+def plan_kernel_count(R: int, S: int, K: int, E: int, B: int) -> int:
+    """Kernels one mep_plan call enqueues for these sizes (launch accounting)."""
+    n = _I(0)
+    _check("mep_plan_kernel_count", load_library().mep_plan_kernel_count(R, S, K, E, B, ctypes.byref(n)))
+    return int(n.value)
 
 
 def grouped_gemm_workspace_bytes(R: int, S: int, K: int, E: int, B: int) -> int:

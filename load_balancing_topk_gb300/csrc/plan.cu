@@ -890,6 +890,26 @@ extern "C" int mep_plan_workspace_bytes(int R, int S, int K, int E, int B, size_
   return MEP_OK;
 }
 
+// Tile groups of the planner's prefix pass and whether k_gsum forms them:
+// beyond 128 KB of tile counts, the group sums are formed by Gs CTAs in
+// parallel rather than inside the one planner CTA.
+static void plan_groups(int nblk, int E, int* Gs, int* tpg, int* presum) {
+  const bool big = (long long)nblk * E >= MEP_PLAN_GSUM_MIN_INTS;
+  tile_groups(nblk, E, big ? kPresumGroups : kMaxScanGroups, Gs, tpg);
+  *presum = big && *Gs > 1 ? 1 : 0;
+}
+
+extern "C" int mep_plan_kernel_count(int R, int S, int K, int E, int B, int* count) {
+  if (count == nullptr) return MEP_ERR_INVALID_ARG;
+  const int rc = plan_check(R, S, K, E, B);
+  if (rc != MEP_OK) return rc;
+  const int nblk = plan_nblk(R, S, K);
+  int Gs, tpg, presum;
+  plan_groups(nblk, E, &Gs, &tpg, &presum);
+  *count = (nblk > 0 ? 2 : 0) + presum + 1;  // k_hist, k_offsets; k_gsum; k_plan
+  return MEP_OK;
+}
+
 static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int B, int fallback,
                        void* workspace, size_t workspace_bytes, int32_t* expert_counts,
                        int32_t* cu_seqlens, int32_t* slot_expert, int32_t* dst_pos,
@@ -925,12 +945,8 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
     return MEP_ERR_CUDA;
 
   if (nblk > 0) k_hist<<<nblk, kTileThreads, hist_smem, st>>>(topk_idx, N, K, E, tpt, ws);
-  // Beyond 128 KB of tile counts, the group sums are formed by Gs CTAs in
-  // parallel rather than inside the one planner CTA.
-  const bool big = (long long)nblk * E >= MEP_PLAN_GSUM_MIN_INTS;
-  int Gs, tpg;
-  tile_groups(nblk, E, big ? kPresumGroups : kMaxScanGroups, &Gs, &tpg);
-  const int presum = big && Gs > 1 ? 1 : 0;
+  int Gs, tpg, presum;
+  plan_groups(nblk, E, &Gs, &tpg, &presum);
   if (presum) {
     const cudaError_t e =
         (E & 3) == 0

@@ -67,9 +67,23 @@ def test_step_bytes():
     assert nb["reduce_grad"] == 2 * (3 + 2) * 2048 * 1408 * 4 + 4 * 64
 
 
+def test_step_bytes_without_gradients():
+    s = synth.LARGE
+    nb = bench.step_bytes(s)
+    assert nb["reduce_grad"] == 0
+    assert nb["total"] == nb["plan"] + nb["dispatch"] + nb["combine"]
+    # dispatch + combine = 2 (1 + K) N H 2 bytes plus the index / weight words
+    assert nb["dispatch"] + nb["combine"] == 2 * (1 + s.K) * s.N * s.H * 2 + 12 * s.A
+
+
 def test_oracle_step_sample_runs_small():
-    r = bench.oracle_step_sample(0.005)
+    s, alpha = bench.medium_workload()
+    r = bench.oracle_step_sample(s, alpha, 0.005, grads=True)
     assert r["bytes"] > 0 and r["seconds"] > 0 and r["n_tok"] == int(32768 * 0.005)
+    s, alpha = bench.headline_workload()
+    r = bench.oracle_step_sample(s, alpha, 0.0005, grads=False)
+    assert r["reduce_s"] < 1e-3 and r["n_tok"] == int(65536 * 0.0005)
+    assert abs(r["maxvio"] - 0.5) < 0.01
 
 
 def test_reference_arm_prints_the_contract_line():
@@ -88,7 +102,7 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"] and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
-    assert line["config"]["workload"].startswith("moe-layer R8 E64 K6 S4096 H2048 B8")
+    assert line["config"]["workload"].startswith("moe-layer R8 E256 K8 S8192 H7168 B32")
 
 
 def test_bench_rejects_short_warmup():
