@@ -570,6 +570,37 @@ def next_rows(args, runner):
     res["prefetch"] = {"ms": round(ms, 4), "gbs": round(nb / ms / 1e6, 1),
                        "frac_of_peak": round(nb / ms / 1e6 / peak, 4), "slots": used,
                        "bytes": nb, "weights": f"bf16 [{s.E}, {synth.GRAD_H}x{synth.GRAD_HP}]"}
+    # the same prefetch inside the step, launched between the plan and the
+    # dispatch (programmatic dependent launch on both sides): its marginal
+    # cost = step time with it - step time without, alternating, medians
+    def step_ms(with_prefetch):
+        runner.reset()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        p = mep.mep_plan(idx_d, s.R, s.S, s.K, s.E, s.B, out=plan)
+        if with_prefetch:
+            mep.mep_prefetch(p.slot_expert, home_w, slot_w, p.status, s.E)
+        mep.mep_dispatch(runner.x_d, p.dst_pos, p.status, s.R, s.S, s.K, buf=buf)
+        mep.mep_combine(buf, w_d, p.dst_pos, p.status, s.R, s.S, s.K, out=out)
+        mep.mep_reduce_grad(p.slot_expert, runner.home_d, runner.slots_d, p.status, s.E)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    with_p, without = [], []
+    for i in range(3 + reps):
+        t1, t0 = step_ms(True), step_ms(False)
+        if i >= 3:
+            with_p.append(t1)
+            without.append(t0)
+    marg = float(np.median(with_p)) - float(np.median(without))
+    res["prefetch_in_step"] = {"marginal_ms": round(marg, 4),
+                               "gbs": round(nb / marg / 1e6, 1) if marg > 0 else None,
+                               "frac_of_peak": round(nb / marg / 1e6 / peak, 4) if marg > 0 else None,
+                               "step_ms_with": round(float(np.median(with_p)), 4),
+                               "step_ms_without": round(float(np.median(without)), 4),
+                               "note": "medium step (plan, dispatch, combine, reduce_grad) with and without "
+                                       "the prefetch between plan and dispatch; medians of 20, alternating"}
     full = torch.from_numpy(synth.full_slot_map(s.E, s.R, s.B, seed=0)).to(dev)
     ms = timed(lambda: mep.mep_prefetch(full, home_w, slot_w, None, s.E))
     nb = 2 * s.R * s.B * HHp * 2

@@ -170,7 +170,8 @@ MEP_API int mep_plan_remote_fallback(const int32_t* topk_idx, int R, int S, int 
  *   slot_w[r][b][:] = home_w[slot_expert[r][b]][:]  for every slot != -1,
  * a byte copy; unused slots are not touched. Any element type.
  *   slot_expert  int32 [R, B]           from mep_plan (or any map into [-1, E))
- *   expert_bytes int64                  bytes of one expert matrix (H*H'*elem), % 16 == 0
+ *   expert_bytes int64                  bytes of one expert matrix (H*H'*elem), % 16 == 0,
+ *                                       at most 32 GiB
  *   home_w       [E, expert_bytes]      home experts' weights (read only)
  *   slot_w       [R, B, expert_bytes]   slot weights (written); must not overlap home_w
  *   status       int32 [1]              read on entry (nonzero: no-op); set to
