@@ -15,15 +15,19 @@
 //              thread.
 //   k_gsum     (large tile tables only) one CTA per group of consecutive
 //              tiles: the group's per-expert sums, so that the planner reads
-//              Gs x E group sums instead of every tile's counts.
+//              Gs x E group sums instead of every tile's counts; it rewrites
+//              each tile's counts as the tile's prefix within its group.
 //   k_plan     one CTA: tile (or group) counts -> T_e and per-group prefixes
-//              (16-byte column loads), home-first keep, overflow pour into
+//              (16-byte column loads; without k_gsum it rewrites the tiles'
+//              in-group prefixes itself), home-first keep, overflow pour into
 //              deficits, slot table, then cu_seqlens and the row bases in
 //              closed form (one parallel pass).
-//   k_offsets  grid over the same tiles: each assignment's index in its
-//              expert's token-ordered list (group prefix + earlier tiles of
-//              the group + warp prefix + rank inside the warp from
-//              __match_any_sync), mapped to its destination row.
+//   k_offsets  grid over the same tiles: before its wait, from the routing
+//              alone, each assignment's rank among the tile's assignments of
+//              its expert (warp prefix + rank inside the warp from
+//              __match_any_sync); after it, the tile's base per expert (group
+//              prefix + in-group prefix) and the planner's tables map it to
+//              its destination row.
 // The planner's rule is home-first: a rank keeps, in expert order, at most
 // S*K of its home experts' tokens; the overflow segments, in expert order,
 // fill the under-loaded ranks' deficits in rank order, one slot per piece.
@@ -51,7 +55,7 @@ constexpr int kMaxScanGroups = MEP_PLAN_SCAN_GROUPS;  // tile groups in k_plan's
 #define MEP_PLAN_PRESUM_GROUPS 16
 #endif
 // groups when k_gsum forms them: fewer, longer groups shorten the planner's
-// scan; each k_offsets tile adds its group's earlier tiles before its wait
+// scan
 constexpr int kPresumGroups = MEP_PLAN_PRESUM_GROUPS;
 constexpr int kPartInts = 8192;              // k_plan shared ints for group sums
 #ifndef MEP_PLAN_GSUM_MIN_INTS
@@ -69,7 +73,8 @@ constexpr int kPartInts = 8192;              // k_plan shared ints for group sum
 inline int tile_tokens(int K) { return (kTileAssign / K) & ~3; }
 
 struct PlanWs {
-  int* blockhist;    // [nblk, E] tile counts
+  int* blockhist;    // [nblk, E] tile counts, rewritten as each tile's exclusive
+                     // prefix within its group (count of e in the group's earlier tiles)
   int* groupbase;    // [Gs, E] count of e in all tiles before group g (Gs <= kMaxScanGroups)
   int* groupsum;     // [Gs, E] count of e in group g (k_gsum; large tile tables only)
   int* blockerr;     // [nblk]
@@ -182,7 +187,7 @@ struct PlanArgs {
   PlanWs ws;
 };
 
-__device__ void plan_fail(const PlanArgs& a, int code, bool zero_counts) {
+__device__ __noinline__ void plan_fail(const PlanArgs& a, int code, bool zero_counts) {
   const int G = a.E + a.B;
   for (int i = threadIdx.x; i < a.R * G; i += blockDim.x) a.cu[i] = 0;
   for (int i = threadIdx.x; i < a.R * a.B; i += blockDim.x) a.slot_expert[i] = -1;
@@ -209,9 +214,10 @@ template <> struct Vec<4> {
 
 // Tiles are split into Gs groups of tpg consecutive tiles (tile_groups()).
 // tile_group_sums: T_e, and for every group g the count of e in all tiles
-// before g (groupbase). Each k_offsets CTA adds the few tiles of its own
-// group that precede it, so no single CTA reads every tile count twice.
-// Columns are W experts wide; thread (g, c) owns group g of column c.
+// before g (groupbase). While summing a group's tiles (when k_gsum has not
+// already), it rewrites each tile's counts as the tile's prefix within the
+// group; a k_offsets CTA adds that row to its group's base. Columns are W
+// experts wide; thread (g, c) owns group g of column c.
 // Row pitch of the shared group sums: odd, so that the column writes of
 // tile_group_sums spread over 8 banks; a single group needs no padding.
 __host__ __device__ inline int part_pitch(int Gs) {
@@ -250,7 +256,7 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT, int* s_e
       for (int j = 0; j < W; ++j) sPart[(c * W + j) * P + g] = Vec<W>::get(v, j);
     }
   } else {
-    const V* h = reinterpret_cast<const V*>(a.ws.blockhist);
+    V* h = reinterpret_cast<V*>(a.ws.blockhist);
     for (int x = tid; x < Gs * nc; x += nthr) {
       const int g = x / nc, c = x - g * nc;
       const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
@@ -259,7 +265,8 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT, int* s_e
       for (int j = 0; j < W; ++j) s[j] = 0;
 #pragma unroll 8
       for (int b = b0; b < b1; ++b) {
-        const V v = h[size_t(b) * nc + c];
+        const V v = __ldcg(h + size_t(b) * nc + c);
+        h[size_t(b) * nc + c] = Vec<W>::make(s);  // the tile's prefix within its group
 #pragma unroll
         for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
       }
@@ -294,18 +301,24 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT, int* s_e
   __syncthreads();
 }
 
+// E % 4 != 0: scalar columns, out of line (see keep_warp0).
+__device__ __noinline__ void tile_group_sums_scalar(const PlanArgs& a, int* sPart, int* sT,
+                                                    int* s_errblk) {
+  tile_group_sums<1>(a, sPart, sT, s_errblk);
+}
+
 // k_gsum: CTA g sums the tile counts of its group of tpg consecutive tiles,
 // W experts per thread (all of a column's tile loads in flight together),
 // into groupsum[g][e].
 template <int W>
 __global__ void __launch_bounds__(kTileThreads)
-    k_gsum(const int* __restrict__ blockhist, int nblk, int E, int tpg, int* __restrict__ groupsum) {
+    k_gsum(int* __restrict__ blockhist, int nblk, int E, int tpg, int* __restrict__ groupsum) {
   pdl_wait();  // k_hist's counts
   pdl_launch_dependents();
   using V = typename Vec<W>::T;
   const int nc = E / W, g = blockIdx.x;
   const int b0 = min(nblk, g * tpg), b1 = min(nblk, b0 + tpg);
-  const V* h = reinterpret_cast<const V*>(blockhist);
+  V* h = reinterpret_cast<V*>(blockhist);
   V* out = reinterpret_cast<V*>(groupsum) + size_t(g) * nc;
   for (int c = threadIdx.x; c < nc; c += blockDim.x) {
     int s[W];
@@ -314,6 +327,7 @@ __global__ void __launch_bounds__(kTileThreads)
 #pragma unroll 8
     for (int b = b0; b < b1; ++b) {
       const V v = __ldcg(h + size_t(b) * nc + c);
+      h[size_t(b) * nc + c] = Vec<W>::make(s);  // the tile's prefix within its group
 #pragma unroll
       for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
     }
@@ -392,34 +406,204 @@ __device__ void warp0_excl_scan(const int* in, int* out, int n) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
-  pdl_wait();                // k_hist's counts and error words
-  pdl_launch_dependents();
+// Shared-memory arrays of k_plan, carved from its dynamic shared memory.
+struct PlanSmem {
+  int *sT, *sPre, *sKeep, *sOv, *sOst, *sOlist, *sFlag, *sPcBeg, *sPcCnt, *sPlen, *sPart, *sDef,
+      *sDst, *sNp, *sPex, *sQ0, *sKpre;
+};
+__device__ __forceinline__ PlanSmem plan_smem(int E, int R) {
   extern __shared__ int smem[];
+  const int EP = E + 1, RP = R + 1;
+  PlanSmem P;
+  P.sT = smem;                    // [E+1]
+  P.sPre = P.sT + EP;             // [E+1]
+  P.sKeep = P.sPre + EP;          // [E+1]
+  P.sOv = P.sKeep + EP;           // [E+1]
+  P.sOst = P.sOv + EP;            // [E+1]
+  P.sOlist = P.sOst + EP;         // [E+1]
+  P.sFlag = P.sOlist + EP;        // [E+1] overflow flags, then their numbering
+  P.sPcBeg = P.sFlag + EP;        // [E+1]
+  P.sPcCnt = P.sPcBeg + EP;       // [E+1]
+  P.sPlen = P.sPcCnt + EP;        // [E+R] piece lengths, by global piece index
+  P.sPart = P.sPlen + E + R;      // [kPartInts] group sums, then the running sum of keep
+  P.sDef = P.sPart + kPartInts;   // [R+1]
+  P.sDst = P.sDef + RP;           // [R+1]
+  P.sNp = P.sDst + RP;            // [R+1]
+  P.sPex = P.sNp + RP;            // [R+1]
+  P.sQ0 = P.sPex + RP;            // [R+1] first overflow segment of each rank
+  P.sKpre = P.sPart;              // [E+1] exclusive prefix of keep, total at E
+  return P;
+}
+
+// The keep / overflow / deficit phase for shapes the one-warp-per-rank pass
+// does not cover. They are kept out of line, with the failure path and the
+// inference-overflow row walk below, so that the path the common shapes take
+// stays one short stretch of code: after an L2 flush every new stretch the
+// planner reaches is fetched from DRAM.
+// Up to 128 experts: warp 0, one pass over chunks of 32 experts (three warp
+// scans per chunk, no block barrier).
+__device__ __noinline__ void keep_warp0(const PlanArgs& a) {
+  const int E = a.E, R = a.R, per = E / R, SK = a.S * a.K;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const PlanSmem P = plan_smem(E, R);
+  int *sT = P.sT, *sPre = P.sPre, *sKeep = P.sKeep, *sOv = P.sOv, *sOst = P.sOst,
+      *sOlist = P.sOlist, *sFlag = P.sFlag, *sDef = P.sDef, *sDst = P.sDst, *sKpre = P.sKpre;
+  if (warp == 0) {
+    int cT = 0, cO = 0, cF = 0, cK = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int T = e < E ? sT[e] : 0;
+      const int iT = warp_incl_scan(T);
+      if (e < E) sPre[e] = cT + iT - T;
+      cT += __shfl_sync(MEP_FULL_MASK, iT, 31);
+      __syncwarp();  // sPre of this chunk visible to the whole warp
+      int ov = 0;
+      if (e < E) {
+        const int r = e / per;
+        const int kp = max(0, min(T, SK - (sPre[e] - sPre[r * per])));
+        ov = T - kp;
+        sKeep[e] = kp;
+        sOv[e] = ov;
+        a.ws.etab[4 * e] = kp;
+      }
+      const int iO = warp_incl_scan(ov);
+      if (e < E) sOst[e] = cO + iO - ov;
+      cO += __shfl_sync(MEP_FULL_MASK, iO, 31);
+      const int kp = e < E ? T - ov : 0;
+      const int iK = warp_incl_scan(kp);
+      if (e < E) sKpre[e] = cK + iK - kp;
+      cK += __shfl_sync(MEP_FULL_MASK, iK, 31);
+      const int f = ov > 0 ? 1 : 0;
+      const int iF = warp_incl_scan(f);
+      if (f) sOlist[cF + iF - 1] = e;
+      cF += __shfl_sync(MEP_FULL_MASK, iF, 31);
+    }
+    if (lane == 0) {
+      sPre[E] = cT;
+      sOst[E] = cO;
+      sFlag[E] = cF;
+      sKpre[E] = cK;
+    }
+    __syncwarp();
+    // deficits S*K - load_r (rank order) and their exclusive running sum
+    int cD = 0;
+    for (int r0 = 0; r0 < R; r0 += 32) {
+      const int r = r0 + lane;
+      const int d = r < R ? max(0, SK - (sPre[(r + 1) * per] - sPre[r * per])) : 0;
+      const int iD = warp_incl_scan(d);
+      if (r < R) {
+        sDef[r] = d;
+        sDst[r] = cD + iD - d;
+      }
+      cD += __shfl_sync(MEP_FULL_MASK, iD, 31);
+    }
+    if (lane == 0) sDst[R] = cD;
+  }
+  __syncthreads();
+}
+
+// Beyond: block-wide scans (faster on GB300 from E = 256 on).
+__device__ __noinline__ void keep_blocks(const PlanArgs& a, int* s_warp) {
+  const int E = a.E, R = a.R, per = E / R, SK = a.S * a.K;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const PlanSmem P = plan_smem(E, R);
+  int *sT = P.sT, *sPre = P.sPre, *sKeep = P.sKeep, *sOv = P.sOv, *sOst = P.sOst,
+      *sOlist = P.sOlist, *sFlag = P.sFlag, *sDef = P.sDef, *sDst = P.sDst, *sKpre = P.sKpre;
+  block_excl_scan(sT, sPre, E, s_warp, true);
+  for (int e = tid; e < E; e += nthr) {
+    const int r = e / per;
+    const int before = sPre[e] - sPre[r * per];
+    const int kp = max(0, min(sT[e], SK - before));
+    sKeep[e] = kp;
+    sOv[e] = sT[e] - kp;
+    sFlag[e] = sOv[e] > 0 ? 1 : 0;
+    a.ws.etab[4 * e] = kp;
+  }
+  __syncthreads();
+  block_excl_scan3(sOv, sOst, sFlag, sFlag, sKeep, sKpre, E, s_warp);
+  for (int e = tid; e < E; e += nthr)
+    if (sOv[e] > 0) sOlist[sFlag[e]] = e;
+  for (int r = tid; r < R; r += nthr)
+    sDef[r] = max(0, SK - (sPre[(r + 1) * per] - sPre[r * per]));
+  __syncthreads();
+  warp0_excl_scan(sDef, sDst, R);
+}
+
+// Inference overflow present (pieces beyond B sit in home rows): cu_seqlens
+// and the row bases by one warp per rank walking its rows in chunks of 32.
+// Row j of rank r: home rows keep their kept count, slot rows E + b hold
+// piece b < B, and pieces b >= B sit in the expert's own row e, found by a
+// binary search over the rank's remaining pieces, whose experts ascend with
+// b. g = the piece, or -1. Out of line (see keep_warp0).
+__device__ __noinline__ void rows_with_overflow(const PlanArgs& a) {
+  const int E = a.E, R = a.R, B = a.B, per = E / R, SK = a.S * a.K, G = E + B;
+  const PlanSmem P = plan_smem(E, R);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int *sKeep = P.sKeep, *sOlist = P.sOlist, *sPlen = P.sPlen, *sNp = P.sNp, *sPex = P.sPex,
+      *sQ0 = P.sQ0;
+  auto row_count = [&](int r, int j, int& g) -> int {
+    g = -1;
+    const int np = sNp[r];
+    if (j < E) {
+      if (j / per == r) return sKeep[j];
+      if (np > B) {
+        const int q0 = sQ0[r];
+        int lo = B, hi = np;
+        while (lo < hi) {
+          const int m = (lo + hi) >> 1;
+          if (sOlist[q0 + m] < j) lo = m + 1; else hi = m;
+        }
+        if (lo < np && sOlist[q0 + lo] == j) {
+          g = sPex[r] + lo;
+          return sPlen[g];
+        }
+      }
+      return 0;
+    }
+    if (j < G && j - E < min(np, B)) {
+      g = sPex[r] + (j - E);
+      return sPlen[g];
+    }
+    return 0;
+  };
+  auto write_row = [&](int r, int j, int c, int g, int incl_end) {
+    a.cu[size_t(r) * G + j] = incl_end;
+    const int start = r * SK + incl_end - c;
+    if (j < E && j / per == r) a.ws.etab[4 * j + 1] = start;
+    else if (g >= 0) a.ws.piece_base[g] = start;
+  };
+  for (int r = warp; r < R; r += nwarps) {
+    int carry = 0;
+    for (int j0 = 0; j0 < G; j0 += 32) {
+      const int j = j0 + lane;
+      int g;
+      const int c = j < G ? row_count(r, j, g) : 0;
+      const int incl = warp_incl_scan(c);
+      if (j < G) write_row(r, j, c, g, carry + incl);
+      carry += __shfl_sync(MEP_FULL_MASK, incl, 31);
+    }
+  }
+}
+
+// The arguments are a __grid_constant__ parameter: the out-of-line helpers
+// read them in place, with no per-thread copy.
+__global__ void __launch_bounds__(kPlanThreads) k_plan(const __grid_constant__ PlanArgs a) {
+  pdl_wait();                // k_hist's counts and error words (k_gsum's group sums)
+  // k_offsets starts now and ranks its tile (from the routing alone) while
+  // this CTA plans. (Releasing it before the wait, while k_hist still runs,
+  // measured 1.2-1.8 us slower at E = 64 and no faster at E = 256.)
+  pdl_launch_dependents();
   const int E = a.E, R = a.R, B = a.B;
   const int per = E / R;
   const int SK = a.S * a.K;
   const int G = E + B;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
-  const int EP = E + 1, RP = R + 1;
-  const int npart = kPartInts;
-  int* sT = smem;                // [E+1]
-  int* sPre = sT + EP;           // [E+1]
-  int* sKeep = sPre + EP;        // [E+1]
-  int* sOv = sKeep + EP;         // [E+1]
-  int* sOst = sOv + EP;          // [E+1]
-  int* sOlist = sOst + EP;       // [E+1]
-  int* sFlag = sOlist + EP;      // [E+1] overflow flags, then their numbering
-  int* sPcBeg = sFlag + EP;      // [E+1]
-  int* sPcCnt = sPcBeg + EP;     // [E+1]
-  int* sPlen = sPcCnt + EP;      // [E+R] piece lengths, by global piece index
-  int* sPart = sPlen + E + R;    // [kPartInts] group sums
-  int* sDef = sPart + npart;     // [R+1]
-  int* sDst = sDef + RP;         // [R+1]
-  int* sNp = sDst + RP;          // [R+1]
-  int* sPex = sNp + RP;          // [R+1]
-  int* sQ0 = sPex + RP;          // [R+1] first overflow segment of each rank
+  const PlanSmem P = plan_smem(E, R);
+  int *sT = P.sT, *sKeep = P.sKeep, *sOv = P.sOv, *sOst = P.sOst, *sOlist = P.sOlist,
+      *sFlag = P.sFlag, *sPcBeg = P.sPcBeg, *sPcCnt = P.sPcCnt, *sPlen = P.sPlen,
+      *sPart = P.sPart, *sDef = P.sDef, *sDst = P.sDst, *sNp = P.sNp, *sPex = P.sPex,
+      *sQ0 = P.sQ0;
   __shared__ int s_warp[3 * 33];
   __shared__ int s_errblk, s_cap, s_over;
 
@@ -431,7 +615,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   // 1. T_e and the per-group prefixes of the tile counts; with them, the
   //    routing errors k_hist found (lowest tile wins)
   if ((E & 3) == 0) tile_group_sums<4>(a, sPart, sT, &s_errblk);
-  else tile_group_sums<1>(a, sPart, sT, &s_errblk);
+  else tile_group_sums_scalar(a, sPart, sT, &s_errblk);
   if (s_errblk != INT_MAX) {
     plan_fail(a, a.ws.blockerr[s_errblk], true);
     return;
@@ -503,77 +687,9 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     }
     __syncthreads();
   } else if (E <= MEP_PLAN_WARP_SCAN_MAX_E) {
-    if (warp == 0) {
-      int cT = 0, cO = 0, cF = 0, cK = 0;
-      for (int e0 = 0; e0 < E; e0 += 32) {
-        const int e = e0 + lane;
-        const int T = e < E ? sT[e] : 0;
-        const int iT = warp_incl_scan(T);
-        if (e < E) sPre[e] = cT + iT - T;
-        cT += __shfl_sync(MEP_FULL_MASK, iT, 31);
-        __syncwarp();  // sPre of this chunk visible to the whole warp
-        int ov = 0;
-        if (e < E) {
-          const int r = e / per;
-          const int kp = max(0, min(T, SK - (sPre[e] - sPre[r * per])));
-          ov = T - kp;
-          sKeep[e] = kp;
-          sOv[e] = ov;
-          a.ws.etab[4 * e] = kp;
-        }
-        const int iO = warp_incl_scan(ov);
-        if (e < E) sOst[e] = cO + iO - ov;
-        cO += __shfl_sync(MEP_FULL_MASK, iO, 31);
-        const int kp = e < E ? T - ov : 0;
-        const int iK = warp_incl_scan(kp);
-        if (e < E) sKpre[e] = cK + iK - kp;
-        cK += __shfl_sync(MEP_FULL_MASK, iK, 31);
-        const int f = ov > 0 ? 1 : 0;
-        const int iF = warp_incl_scan(f);
-        if (f) sOlist[cF + iF - 1] = e;
-        cF += __shfl_sync(MEP_FULL_MASK, iF, 31);
-      }
-      if (lane == 0) {
-        sPre[E] = cT;
-        sOst[E] = cO;
-        sFlag[E] = cF;
-        sKpre[E] = cK;
-      }
-      __syncwarp();
-      // deficits S*K - load_r (rank order) and their exclusive running sum
-      int cD = 0;
-      for (int r0 = 0; r0 < R; r0 += 32) {
-        const int r = r0 + lane;
-        const int d = r < R ? max(0, SK - (sPre[(r + 1) * per] - sPre[r * per])) : 0;
-        const int iD = warp_incl_scan(d);
-        if (r < R) {
-          sDef[r] = d;
-          sDst[r] = cD + iD - d;
-        }
-        cD += __shfl_sync(MEP_FULL_MASK, iD, 31);
-      }
-      if (lane == 0) sDst[R] = cD;
-    }
-    __syncthreads();
+    keep_warp0(a);
   } else {
-    block_excl_scan(sT, sPre, E, s_warp, true);
-    for (int e = tid; e < E; e += nthr) {
-      const int r = e / per;
-      const int before = sPre[e] - sPre[r * per];
-      const int kp = max(0, min(sT[e], SK - before));
-      sKeep[e] = kp;
-      sOv[e] = sT[e] - kp;
-      sFlag[e] = sOv[e] > 0 ? 1 : 0;
-      a.ws.etab[4 * e] = kp;
-    }
-    __syncthreads();
-    block_excl_scan3(sOv, sOst, sFlag, sFlag, sKeep, sKpre, E, s_warp);
-    for (int e = tid; e < E; e += nthr)
-      if (sOv[e] > 0) sOlist[sFlag[e]] = e;
-    for (int r = tid; r < R; r += nthr)
-      sDef[r] = max(0, SK - (sPre[(r + 1) * per] - sPre[r * per]));
-    __syncthreads();
-    warp0_excl_scan(sDef, sDst, R);
+    keep_blocks(a, s_warp);
   }
   const int nov = sFlag[E];
 
@@ -651,41 +767,6 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
   }
 
   // 5. cu_seqlens; also the global first row of every home row and piece.
-  //    Row j of rank r: home rows keep their kept count, slot rows E + b
-  //    hold piece b < B, and pieces b >= B (fallback only) sit in the
-  //    expert's own row e, found by a binary search over the rank's
-  //    remaining pieces, whose experts ascend with b. g = the piece, or -1.
-  auto row_count = [&](int r, int j, int& g) -> int {
-    g = -1;
-    const int np = sNp[r];
-    if (j < E) {
-      if (j / per == r) return sKeep[j];
-      if (np > B) {
-        const int q0 = sQ0[r];
-        int lo = B, hi = np;
-        while (lo < hi) {
-          const int m = (lo + hi) >> 1;
-          if (sOlist[q0 + m] < j) lo = m + 1; else hi = m;
-        }
-        if (lo < np && sOlist[q0 + lo] == j) {
-          g = sPex[r] + lo;
-          return sPlen[g];
-        }
-      }
-      return 0;
-    }
-    if (j < G && j - E < min(np, B)) {
-      g = sPex[r] + (j - E);
-      return sPlen[g];
-    }
-    return 0;
-  };
-  auto write_row = [&](int r, int j, int c, int g, int incl_end) {
-    a.cu[size_t(r) * G + j] = incl_end;
-    const int start = r * SK + incl_end - c;
-    if (j < E && j / per == r) a.ws.etab[4 * j + 1] = start;
-    else if (g >= 0) a.ws.piece_base[g] = start;
-  };
   if (!s_over) {
     // Every piece sits in a slot row (no inference overflow), so every entry
     // has a closed form and all R x (E+B) are written in one parallel pass.
@@ -713,18 +794,7 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(PlanArgs a) {
     if (tid == 0) *a.status = MEP_OK;
     return;
   }
-  // inference overflow present: one warp per rank, its chunks of 32 rows in order
-  for (int r = warp; r < R; r += nwarps) {
-    int carry = 0;
-    for (int j0 = 0; j0 < G; j0 += 32) {
-      const int j = j0 + lane;
-      int g;
-      const int c = j < G ? row_count(r, j, g) : 0;
-      const int incl = warp_incl_scan(c);
-      if (j < G) write_row(r, j, c, g, carry + incl);
-      carry += __shfl_sync(MEP_FULL_MASK, incl, 31);
-    }
-  }
+  rows_with_overflow(a);
   if (tid == 0) *a.status = MEP_OK;
 }
 
@@ -746,9 +816,11 @@ __global__ void __launch_bounds__(kTileThreads)
   const int ntok = min(tok_per_tile, N - t0);
   const int na = ntok * K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // Everything up to the wait depends only on the routing and on k_hist, so
-  // it overlaps the planner: stage the tile, then rank each assignment among
-  // the tile's assignments of the same expert.
+  // Everything up to the wait depends only on the routing (an input, complete
+  // before k_hist started), so it overlaps the histogram and the planner:
+  // stage the tile, then rank each assignment among the tile's assignments
+  // of the same expert. Nothing an earlier kernel of the plan writes is read
+  // before the wait.
   {
     const int32_t* g = topk_idx + size_t(t0) * K;
     const int nv = na >> 2;
@@ -790,15 +862,11 @@ __global__ void __launch_bounds__(kTileThreads)
   }
   __syncthreads();
 
-  // The tile's offsets from its group's base need no wait either: the
-  // group's earlier tiles come from k_hist, which has completed before this
-  // grid can start (the planner releases it only after its own wait on
-  // k_hist). Then each assignment's expert and offset go to registers.
+  // Each warp's counts become exclusive offsets within the tile; then each
+  // assignment's expert and tile-relative offset go to registers.
   const int g = blk / tpg;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
-#pragma unroll 8
-    for (int b = g * tpg; b < blk; ++b) run += __ldcg(ws.blockhist + size_t(b) * E + e);
 #pragma unroll
     for (int w = 0; w < kTileWarps; ++w) {
       const int v = s_wcnt[w * E + e];
@@ -821,14 +889,17 @@ __global__ void __launch_bounds__(kTileThreads)
   pdl_wait();                           // the planner's tables and status
   pdl_launch_dependents();
   const int st = status != nullptr ? __ldcg(status) : 0;
-  // Per expert, with this group's base gb folded in: a kept token's row is
-  // home_base + gb + rel, for rel < keep - gb (one 8-byte shared load on the
-  // common path); the rest go through the expert's pieces.
+  // Per expert, with this tile's base gb (the count of e in all earlier
+  // tiles: its group's base from the planner plus the tile's prefix within
+  // the group) folded in: a kept token's row is home_base + gb + rel, for
+  // rel < keep - gb (one 8-byte shared load on the common path); the rest go
+  // through the expert's pieces.
   int2* s_fast = reinterpret_cast<int2*>(s_wcnt);  // [E] {home_base + gb, keep - gb}
   int2* s_slow = s_fast + E;                       // [E] {gb, first piece | pieces << 16}
   const int4* etab = reinterpret_cast<const int4*>(ws.etab);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int gb = __ldcg(ws.groupbase + size_t(g) * E + e);
+    const int gb = __ldcg(ws.groupbase + size_t(g) * E + e) +
+                   __ldcg(ws.blockhist + size_t(blk) * E + e);
     const int4 t = __ldcg(etab + e);
     s_fast[e] = make_int2(t.y + min(gb, t.x), t.x - gb);  // (no kept token left: unused base)
     s_slow[e] = make_int2(gb, t.z | (t.w << 16));
@@ -956,9 +1027,9 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
     const cudaError_t e =
         (E & 3) == 0
             ? launch_pdl(k_gsum<4>, dim3(Gs), dim3(kTileThreads), 0, st,
-                         static_cast<const int*>(ws.blockhist), nblk, E, tpg, ws.groupsum)
+                         ws.blockhist, nblk, E, tpg, ws.groupsum)
             : launch_pdl(k_gsum<1>, dim3(Gs), dim3(kTileThreads), 0, st,
-                         static_cast<const int*>(ws.blockhist), nblk, E, tpg, ws.groupsum);
+                         ws.blockhist, nblk, E, tpg, ws.groupsum);
     if (e != cudaSuccess) return MEP_ERR_CUDA;
   }
   PlanArgs pa{nblk,          R,          S,           K,      E,  B, fallback, presum, Gs, tpg,
