@@ -800,17 +800,20 @@ def _sample_text(r, s, frac, grads, seconds):
             f"of them{g}; single-threaded C oracle, {seconds:.1f} s")
 
 
-def cpu_baseline(s, alpha, grads, budget_s: float = 12.0) -> dict:
+def cpu_baseline(s, alpha, grads, budget_s: float = 16.0) -> dict:
     """The oracle timed on about budget_s of CPU work: a token fraction of one
     step while one step would take longer, else whole steps repeated."""
     probe = oracle_step_sample(s, alpha, 0.01, grads)
-    frac = min(1.0, 0.01 * budget_s / max(probe["seconds"], 1e-3) / 2.0)
-    r = oracle_step_sample(s, alpha, frac, grads)
-    if frac == 1.0 and r["seconds"] < budget_s:
-        reps = max(1, int(round((budget_s - r["seconds"]) / max(r["seconds"], 1e-3))))
-        more = oracle_step_sample(s, alpha, 1.0, grads, reps=reps)
-        r = dict(more, bytes=more["bytes"] + r["bytes"], seconds=more["seconds"] + r["seconds"],
-                 reps=reps + 1)
+    # the plan runs in full at any fraction; the rest scales with the tokens
+    per_full = (probe["seconds"] - probe["plan_s"]) / 0.01
+    frac = max(0.01, (budget_s - probe["plan_s"]) / max(per_full, 1e-3))
+    if frac >= 1.0:  # whole steps fit the budget: repeat them
+        one = oracle_step_sample(s, alpha, 1.0, grads)
+        reps = max(1, int(round(budget_s / max(one["seconds"], 1e-3))))
+        frac = 1.0
+        r = oracle_step_sample(s, alpha, 1.0, grads, reps=reps) if reps > 1 else one
+    else:
+        r = oracle_step_sample(s, alpha, frac, grads)
     return {"value": round(r["bytes"] / r["seconds"] / 1e9, 3), "unit": "GB/s", "cores": 1,
             "host_cores": _host_cores(), "kind": "oracle",
             "sample": _sample_text(r, s, frac, grads, r["seconds"])}
