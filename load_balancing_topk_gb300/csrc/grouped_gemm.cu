@@ -86,9 +86,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -215,8 +212,13 @@ __device__ __forceinline__ void tc_commit2(uint32_t bar) {
 }
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes, one lane (row)
-// per thread.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+// per thread: tc_ld32_issue starts the load; tc_ld_wait waits for all of
+// this thread's loads so far and then ties v to that wait (an empty asm
+// that "rewrites" v), so that no use of v can be scheduled above it.
+// (Keeping the next chunk's load in flight while one is stored measured the
+// same: the epilogue's time goes to its stores, and it overlaps the next
+// unit's MMAs through the second accumulator.)
+__device__ __forceinline__ void tc_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
       "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
@@ -227,7 +229,10 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
+}
+__device__ __forceinline__ void tc_ld_wait(uint32_t (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  asm volatile("" : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
@@ -502,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16* out = y + ((long long)t.x + r) * Hp + n0;
       for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
         uint32_t v[32];
-        tc_ld32(tmem + a * kBN + 32 * c + ((uint32_t)(32 * q) << 16), v);
+        tc_ld32_issue(tmem + a * kBN + 32 * c + ((uint32_t)(32 * q) << 16), v);
+        tc_ld_wait(v);
         if (row_ok) store_chunk(out + 32 * c, v, Hp - (n0 + 32 * c), st32);
       }
       tc_fence_before();
