@@ -633,8 +633,9 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const __grid_constant__ P
   if (MEP_PLAN_RANK_WARPS && per <= 32 && R <= nwarps) {
     // Warp r holds rank r's home experts, one per lane: the keep, overflow,
     // flag and keep prefixes inside the rank are warp scans, and the rank's
-    // load gives its deficit. Warp 0 then scans the R rank totals (and the
-    // deficits), and each warp adds its rank's offsets: two block barriers.
+    // load gives its deficit. After one block barrier every rank's warp scans
+    // the R rank totals itself and adds its own offsets (warp 0 also the
+    // deficits' running sum): two block barriers in all.
     const int r = warp, e = r * per + lane;
     const bool in = r < R && lane < per;
     int ov = 0, f = 0, kp = 0, exO = 0, exF = 0, exK = 0;
@@ -661,29 +662,30 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const __grid_constant__ P
       }
     }
     __syncthreads();
-    if (warp == 0) {
-#pragma unroll
-      for (int q = 0; q < 3; ++q) {
-        const int v = lane < R ? s_warp[33 * q + lane] : 0;
-        const int vi = warp_incl_scan(v);
-        s_warp[33 * q + lane] = vi - v;
-        if (lane == 31) s_warp[33 * q + 32] = vi;
+    if (r < R) {
+      const int vO = lane < R ? s_warp[lane] : 0;
+      const int vF = lane < R ? s_warp[33 + lane] : 0;
+      const int vK = lane < R ? s_warp[66 + lane] : 0;
+      const int iO = warp_incl_scan(vO), iF = warp_incl_scan(vF), iK = warp_incl_scan(vK);
+      const int bO = __shfl_sync(MEP_FULL_MASK, iO - vO, r);  // this rank's exclusive offsets
+      const int bF = __shfl_sync(MEP_FULL_MASK, iF - vF, r);
+      const int bK = __shfl_sync(MEP_FULL_MASK, iK - vK, r);
+      if (in) {
+        sOst[e] = bO + exO;
+        if (f) sOlist[bF + exF] = e;
+        sKpre[e] = bK + exK;
       }
-      const int d = lane < R ? sDef[lane] : 0;
-      const int iD = warp_incl_scan(d);
-      if (lane < R) sDst[lane] = iD - d;
-      if (lane == 31) sDst[R] = iD;
-    }
-    __syncthreads();
-    if (in) {
-      sOst[e] = s_warp[r] + exO;
-      if (f) sOlist[s_warp[33 + r] + exF] = e;
-      sKpre[e] = s_warp[66 + r] + exK;
-    }
-    if (tid == 0) {
-      sOst[E] = s_warp[32];
-      sFlag[E] = s_warp[65];
-      sKpre[E] = s_warp[98];
+      if (r == 0) {
+        const int d = lane < R ? sDef[lane] : 0;
+        const int iD = warp_incl_scan(d);
+        if (lane < R) sDst[lane] = iD - d;
+        if (lane == 31) {  // the totals
+          sDst[R] = iD;
+          sOst[E] = iO;
+          sFlag[E] = iF;
+          sKpre[E] = iK;
+        }
+      }
     }
     __syncthreads();
   } else if (E <= MEP_PLAN_WARP_SCAN_MAX_E) {
@@ -701,40 +703,64 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const __grid_constant__ P
     sPcBeg[e] = INT_MAX;
     sPcCnt[e] = 0;
   }
-  for (int r = tid; r < R; r += nthr) {
-    int np = 0, q0 = 0;
+  // Rank r's pieces: the segments tile the overflow line in order, so the
+  // ones meeting [lo, hi) are those from the first ending after lo up to
+  // (not including) the first starting at or after hi: two binary searches.
+  auto count_pieces = [&](int r, int& q0) -> int {
+    q0 = 0;
     const int d = sDef[r];
-    if (d > 0) {
-      // the segments tile the overflow line in order, so the ones meeting
-      // [lo, hi) are those from the first ending after lo up to (not
-      // including) the first starting at or after hi: two binary searches
-      const int lo = sDst[r], hi = lo + d;
-      int q1 = nov;
-      while (q0 < q1) {
-        const int m = (q0 + q1) >> 1;
-        const int e = sOlist[m];
-        if (sOst[e] + sOv[e] > lo) q1 = m; else q0 = m + 1;
-      }
-      int q2 = q0, q3 = nov;
-      while (q2 < q3) {
-        const int m = (q2 + q3) >> 1;
-        if (sOst[sOlist[m]] >= hi) q3 = m; else q2 = m + 1;
-      }
-      np = q2 - q0;
+    if (d <= 0) return 0;
+    const int lo = sDst[r], hi = lo + d;
+    int q1 = nov;
+    while (q0 < q1) {
+      const int m = (q0 + q1) >> 1;
+      const int e = sOlist[m];
+      if (sOst[e] + sOv[e] > lo) q1 = m; else q0 = m + 1;
     }
-    if (np > B) {
-      if (!a.fallback) s_cap = 1;
-      s_over = 1;  // inference: pieces beyond B sit in home rows
+    int q2 = q0, q3 = nov;
+    while (q2 < q3) {
+      const int m = (q2 + q3) >> 1;
+      if (sOst[sOlist[m]] >= hi) q3 = m; else q2 = m + 1;
     }
-    sNp[r] = np;
-    sQ0[r] = q0;
+    return q2 - q0;
+  };
+  if (R <= 32) {
+    // warp 0, one rank per lane: count, flag, and number the pieces (a warp
+    // scan) with no block barrier in between
+    if (warp == 0) {
+      int q0 = 0;
+      const int np = lane < R ? count_pieces(lane, q0) : 0;
+      if (__any_sync(MEP_FULL_MASK, np > B) && lane == 0) {
+        if (!a.fallback) s_cap = 1;
+        s_over = 1;  // inference: pieces beyond B sit in home rows
+      }
+      const int incl = warp_incl_scan(np);
+      if (lane < R) {
+        sNp[lane] = np;
+        sQ0[lane] = q0;
+        sPex[lane] = incl - np;
+      }
+      if (lane == 31) sPex[R] = incl;  // pieces in all
+    }
+    __syncthreads();
+  } else {
+    for (int r = tid; r < R; r += nthr) {
+      int q0;
+      const int np = count_pieces(r, q0);
+      if (np > B) {
+        if (!a.fallback) s_cap = 1;
+        s_over = 1;
+      }
+      sNp[r] = np;
+      sQ0[r] = q0;
+    }
+    __syncthreads();
+    warp0_excl_scan(sNp, sPex, R);  // sPex[R]: pieces in all
   }
-  __syncthreads();
   if (s_cap) {
     plan_fail(a, MEP_ERR_CAPACITY, false);
     return;
   }
-  warp0_excl_scan(sNp, sPex, R);  // sPex[R]: pieces in all
   // slot table, one thread per (rank, slot): the rank's b-th piece's expert,
   // or -1 (pieces beyond B, inference only, have no slot)
   for (int i = tid; i < R * B; i += nthr) {
