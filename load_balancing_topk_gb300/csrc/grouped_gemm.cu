@@ -29,10 +29,13 @@
 //                 commit is multicast to both CTAs (stage free, accumulator
 //                 ready);
 //     warps 2..5  epilogue of each CTA: tcgen05.ld of its 128 TMEM lanes
-//                 (= its tile's rows), bf16 (nearest-even), whole-sector
-//                 stores of the valid rows and columns, then a release on CTA 0's
-//                 accumulator barrier; the accumulator is double-buffered,
-//                 so the next unit's MMAs overlap this store.
+//                 (= its tile's rows), bf16 (nearest-even); a warp whose 32
+//                 rows are all valid writes them through shared memory (two
+//                 4 KB boxes in the y map's swizzled layout, alternating) with
+//                 bulk tensor stores, a warp with padding rows stores its
+//                 valid rows lane by lane (whole sectors); then a release on
+//                 CTA 0's accumulator barrier. The accumulator is
+//                 double-buffered, so the next unit's MMAs overlap this store.
 // Every wait is bounded (MEP_GEMM_TIMEOUT_NS on %globaltimer): a wait that
 // gives up raises a CTA-wide abort flag and MEP_ERR_TIMEOUT; every role then
 // leaves its loop, the producer waits for its own copies in flight, the MMA
@@ -143,6 +146,25 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
       : "memory");
 }
+// Bulk tensor store of one 64-column x 32-row box of y from shared memory
+// (128-byte swizzle, the layout of the tensor map); columns at or beyond the
+// map's width are not written. Each store is its own bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n\t"
+      "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+// Wait until at most one of this thread's bulk stores still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// Wait until all of this thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Address of the same shared variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -339,7 +361,9 @@ __global__ void __launch_bounds__(kTileThreads)
 #define MEP_GEMM_PAIR_STAGES 5
 #endif
 constexpr int kStages2 = MEP_GEMM_PAIR_STAGES;  // ring depth of the CTA-pair kernel (32 KB stages)
-constexpr int kSmemPair = 1024 /* alignment slack */ + kStages2 * (kABytes + 2 * kBBox) + 256;
+constexpr int kStoreBox = 32 * 64 * 2;  // one epilogue warp's 32 rows x 64 columns of y, bf16: 4 KB
+constexpr int kStaging = 4 * 2 * kStoreBox;  // two staging boxes per epilogue warp, 4 warps: 32 KB
+constexpr int kSmemPair = 1024 /* alignment slack */ + kStages2 * (kABytes + 2 * kBBox) + kStaging + 256;
 static_assert(kSmemPair <= 232448, "the CTA-pair ring must fit in 227 KB of shared memory");
 struct GemmSmem {
   uint64_t full[kStages2], empty[kStages2], tfull[2], tempty[2], drain;
@@ -361,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_wh,
                 const __grid_constant__ CUtensorMap map_ws, const int4* __restrict__ tiles,
                 const int* __restrict__ count_ptr, int32_t* status, int E, int H, int Hp,
-                __nv_bfloat16* __restrict__ y, int st32_flag) {
+                __nv_bfloat16* __restrict__ y, int st32_flag,
+                const __grid_constant__ CUtensorMap map_y) {
   constexpr int kSt = kStages2;
   const bool st32 = st32_flag != 0;
   constexpr int kBHalf = 2 * kBBox;  // 128 weight columns per CTA per stage
@@ -371,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gen_base = smem_raw + (base - raw);
   const uint32_t sa = base;
   const uint32_t sb = base + kSt * kABytes;
-  GemmSmem* S = reinterpret_cast<GemmSmem*>(gen_base + kSt * (kABytes + kBHalf));
+  const uint32_t sy = base + kSt * (kABytes + kBHalf);  // epilogue staging, 1024-byte aligned
+  GemmSmem* S = reinterpret_cast<GemmSmem*>(gen_base + kSt * (kABytes + kBHalf) + kStaging);
   volatile int* abort_flag = &S->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -494,8 +520,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
+    // Warp q owns TMEM lanes (= tile rows) [32q, 32q + 32). When all 32 of
+    // its rows are valid, each 64-column box goes TMEM -> registers -> bf16
+    // -> shared memory (the 128-byte swizzled layout of the y map) -> one
+    // bulk tensor store, alternating two staging boxes; otherwise each lane
+    // stores its own row.
     const int q = warp & 3;
-    uint32_t lt = 0;
+    const uint32_t stage0 = sy + (uint32_t)q * 2 * kStoreBox;
+    uint32_t lt = 0, nbox = 0;
     for (long long u = u0; u < units; u += ustep, ++lt) {
       const uint32_t a = lt & 1u, use = lt >> 1;
       if (!wait_phase(smem_u32(&S->tfull[a]), use & 1u, abort_flag, status)) break;
@@ -503,18 +535,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int4 t = tiles[(u / nN) * 2 + rank];
       const int n0 = int(u % nN) * kBN;
       const int r = 32 * q + lane;
-      const bool row_ok = r < t.y;
-      __nv_bfloat16* out = y + ((long long)t.x + r) * Hp + n0;
-      for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
-        uint32_t v[32];
-        tc_ld32_issue(tmem + a * kBN + 32 * c + ((uint32_t)(32 * q) << 16), v);
-        tc_ld_wait(v);
-        if (row_ok) store_chunk(out + 32 * c, v, Hp - (n0 + 32 * c), st32);
+      const uint32_t ta = tmem + a * kBN + ((uint32_t)(32 * q) << 16);
+      if (t.y >= 32 * q + 32) {
+        for (int i = 0; i < kBN / 64 && n0 + 64 * i < Hp; ++i, ++nbox) {
+          const uint32_t box = stage0 + (nbox & 1u) * kStoreBox;
+          if (lane == 0) bulk_wait_read_1();  // the store that last used this box has read it
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = 2 * i + h;  // 32-column chunk
+            if (n0 + 32 * c >= Hp) break;
+            uint32_t v[32];
+            tc_ld32_issue(ta + 32 * c, v);
+            tc_ld_wait(v);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // 16-byte piece 4h + j of this row's 128 bytes
+              const uint32_t off = (uint32_t)lane * 128u +
+                                   ((uint32_t)((4 * h + j) ^ (lane & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(box + off),
+                           "r"(pack_bf16(v[8 * j + 0], v[8 * j + 1])),
+                           "r"(pack_bf16(v[8 * j + 2], v[8 * j + 3])),
+                           "r"(pack_bf16(v[8 * j + 4], v[8 * j + 5])),
+                           "r"(pack_bf16(v[8 * j + 6], v[8 * j + 7]))
+                           : "memory");
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&map_y, n0 + 64 * i, t.x + 32 * q, box);
+        }
+      } else {
+        const bool row_ok = r < t.y;  // padding tiles have no rows
+        __nv_bfloat16* out = y + ((long long)t.x + r) * Hp + n0;
+        for (int c = 0; c < kBN / 32 && n0 + 32 * c < Hp; ++c) {
+          uint32_t v[32];
+          tc_ld32_issue(ta + 32 * c, v);
+          tc_ld_wait(v);
+          if (row_ok) store_chunk(out + 32 * c, v, Hp - (n0 + 32 * c), st32);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&S->tempty[a]), 0));
     }
+    if (lane == 0) bulk_wait_all();  // every bulk store of this warp has completed
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -617,7 +682,7 @@ template <typename Kernel>
 cudaError_t launch_gemm(Kernel kernel, int CL, int smem, GridCache& cache, cudaStream_t st,
                         const CUtensorMap& mx, const CUtensorMap& mh, const CUtensorMap& msl,
                         const int4* tiles, const int* count, int32_t* status, int E, int H,
-                        int Hp, __nv_bfloat16* y, int st32) {
+                        int Hp, __nv_bfloat16* y, int st32, const CUtensorMap& my) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -647,7 +712,7 @@ cudaError_t launch_gemm(Kernel kernel, int CL, int smem, GridCache& cache, cudaS
     grid = cache.grid[dev];
   }
   cfg.gridDim = dim3(grid);
-  return cudaLaunchKernelEx(&cfg, kernel, mx, mh, msl, tiles, count, status, E, H, Hp, y, st32);
+  return cudaLaunchKernelEx(&cfg, kernel, mx, mh, msl, tiles, count, status, E, H, Hp, y, st32, my);
 }
 
 }  // namespace
@@ -685,8 +750,9 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
   if (!on_current_device(x) || !on_current_device(w_home) || !on_current_device(y) ||
       (B > 0 && !on_current_device(w_slot)))
     return MEP_ERR_INVALID_ARG;
-  CUtensorMap mx, mh, msl;
-  if (!make_map(&mx, x, (unsigned long long)rows, (unsigned long long)H, kBM) ||
+  CUtensorMap mx, mh, msl, my;
+  if (!make_map(&my, y, (unsigned long long)rows, (unsigned long long)Hp, 32) ||
+      !make_map(&mx, x, (unsigned long long)rows, (unsigned long long)H, kBM) ||
       !make_map(&mh, w_home, (unsigned long long)E * H, (unsigned long long)Hp, kBK))
     return MEP_ERR_CUDA;
   if (B > 0) {
@@ -708,7 +774,7 @@ extern "C" int mep_grouped_gemm(const mep_bf16* x, const int32_t* cu_seqlens,
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_gemm_pair), kSmemPair))
     return MEP_ERR_CUDA;
   err = launch_gemm(k_gemm_pair, kPair, kSmemPair, cache, st, mx, mh, msl, tiles, count, status, E,
-                    H, Hp, yb, st32);
+                    H, Hp, yb, st32, my);
   return err == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
 
