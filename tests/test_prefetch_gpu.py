@@ -75,3 +75,23 @@ def test_prefetch_bad_map_and_status():
     mep.mep_prefetch(to_dev(np.array([[0, 3], [1, -1]], np.int32)), to_dev(home), sd, status, E)
     torch.cuda.synchronize()
     assert (to_np(sd) == 0).all()
+
+
+@pytest.mark.parametrize("R,B,E,n,frac", [
+    (1024, 32, 4096, 8, 0.6),     # R*B = 32768, the slot limit; expert ids up to 4095; 16-byte experts
+    (64, 64, 4096, 24, 0.3),      # 4096 slots, experts of 48 bytes: every item spans many slots
+    (16, 24, 384, 520, 0.9),      # experts of 1040 bytes (65 vectors): items cross slot boundaries
+])
+def test_prefetch_large_slot_maps(R, B, E, n, frac):
+    """Slot maps far larger than a plan's: the used slots are listed by every
+    CTA (one part of the map per warp), their vectors cut into equal items that
+    cross from slot to slot; the largest expert id and the largest slot id
+    both occur. Unused slots must stay untouched."""
+    rng = np.random.default_rng([R, B, E, n])
+    se = rng.integers(0, E, size=(R, B), dtype=np.int32)
+    se[rng.random((R, B)) > frac] = -1
+    se[0, 0] = E - 1
+    se[R - 1, B - 1] = E - 1
+    home = _bf16_weights(E, n, 6)
+    slot = _bf16_weights(R * B, n, 7)
+    assert check(se, home, slot, E) == "ok"
