@@ -438,8 +438,9 @@ __device__ __forceinline__ PlanSmem plan_smem(int E, int R) {
 // The keep / overflow / deficit phase for shapes the one-warp-per-rank pass
 // does not cover. They are kept out of line, with the failure path and the
 // inference-overflow row walk below, so that the path the common shapes take
-// stays one short stretch of code: after an L2 flush every new stretch the
-// planner reaches is fetched from DRAM.
+// is one short stretch of code. (Measured about even against the inlined
+// form; running the planner twice in one CTA showed that instruction fetch
+// is not what its time goes to.)
 // Up to 128 experts: warp 0, one pass over chunks of 32 experts (three warp
 // scans per chunk, no block barrier).
 __device__ __noinline__ void keep_warp0(const PlanArgs& a) {
