@@ -231,8 +231,9 @@ inline void tile_groups(int nblk, int E, int max_groups, int* Gs, int* tpg) {
   int g = nblk < max_groups ? nblk : max_groups;
   while (g > 1 && E * part_pitch(g) > kPartInts) --g;
   if (g < 1) g = 1;
-  *Gs = g;
   *tpg = nblk > 0 ? (nblk + g - 1) / g : 1;
+  // only the groups that hold tiles (97 tiles in groups of 2: 49, not 64)
+  *Gs = nblk > 0 ? (nblk + *tpg - 1) / *tpg : 1;
 }
 
 // Also collects k_hist's error words: their loads go out with the counts,
