@@ -171,7 +171,7 @@ MEP_API int mep_plan_remote_fallback(const int32_t* topk_idx, int R, int S, int 
  * a byte copy; unused slots are not touched. Any element type.
  *   slot_expert  int32 [R, B]           from mep_plan (or any map into [-1, E))
  *   expert_bytes int64                  bytes of one expert matrix (H*H'*elem), % 16 == 0,
- *                                       at most 32 GiB
+ *                                       below 32 GiB (expert_bytes / 16 < 2^31 - 256)
  *   home_w       [E, expert_bytes]      home experts' weights (read only)
  *   slot_w       [R, B, expert_bytes]   slot weights (written); must not overlap home_w
  *   status       int32 [1]              read on entry (nonzero: no-op); set to

@@ -169,8 +169,10 @@ using namespace mep;
 
 extern "C" int mep_prefetch(const int32_t* slot_expert, int E, int R, int B, int64_t expert_bytes,
                             const void* home_w, void* slot_w, int32_t* status, void* stream) {
+  // in-slot vector offsets are 32-bit and reach nvec + 2 * kThreads before
+  // they wrap into the next slot: keep that below 2^31
   if (E < 1 || E > MEP_MAX_E || R < 1 || B < 0 || expert_bytes < 0 || expert_bytes % 16 != 0 ||
-      expert_bytes / 16 > 0x7fffffffLL)
+      expert_bytes / 16 > 0x7fffffffLL - 2 * kThreads)
     return MEP_ERR_INVALID_ARG;
   if ((long long)R * B > MEP_MAX_SLOTS) return MEP_ERR_INVALID_ARG;
   const int RB = R * B;
