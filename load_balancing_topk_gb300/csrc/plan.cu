@@ -212,6 +212,30 @@ template <> struct Vec<4> {
   }
 };
 
+// Column c of tiles [b0, b1): adds their counts to s and rewrites each tile's
+// counts as its prefix within the range (the sum of the earlier tiles). The
+// loads of a batch of NB tiles all go out before any of their stores: each
+// store writes the array the next load reads, so a load-store-load order
+// would wait one L2 round trip per tile.
+template <int W, int NB>
+__device__ __forceinline__ void prefix_tiles(typename Vec<W>::T* h, int nc, int c, int b0, int b1,
+                                             int (&s)[W]) {
+  using V = typename Vec<W>::T;
+  for (int b = b0; b < b1; b += NB) {
+    V v[NB];
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+      if (b + i < b1) v[i] = __ldcg(h + size_t(b + i) * nc + c);
+#pragma unroll
+    for (int i = 0; i < NB; ++i)
+      if (b + i < b1) {
+        h[size_t(b + i) * nc + c] = Vec<W>::make(s);
+#pragma unroll
+        for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v[i], j);
+      }
+  }
+}
+
 // Tiles are split into Gs groups of tpg consecutive tiles (tile_groups()).
 // tile_group_sums: T_e, and for every group g the count of e in all tiles
 // before g (groupbase). While summing a group's tiles (when k_gsum has not
@@ -264,13 +288,7 @@ __device__ void tile_group_sums(const PlanArgs& a, int* sPart, int* sT, int* s_e
       int s[W];
 #pragma unroll
       for (int j = 0; j < W; ++j) s[j] = 0;
-#pragma unroll 8
-      for (int b = b0; b < b1; ++b) {
-        const V v = __ldcg(h + size_t(b) * nc + c);
-        h[size_t(b) * nc + c] = Vec<W>::make(s);  // the tile's prefix within its group
-#pragma unroll
-        for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
-      }
+      prefix_tiles<W, 4>(h, nc, c, b0, b1, s);
 #pragma unroll
       for (int j = 0; j < W; ++j) sPart[(c * W + j) * P + g] = s[j];
     }
@@ -325,13 +343,7 @@ __global__ void __launch_bounds__(kTileThreads)
     int s[W];
 #pragma unroll
     for (int j = 0; j < W; ++j) s[j] = 0;
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) {
-      const V v = __ldcg(h + size_t(b) * nc + c);
-      h[size_t(b) * nc + c] = Vec<W>::make(s);  // the tile's prefix within its group
-#pragma unroll
-      for (int j = 0; j < W; ++j) s[j] += Vec<W>::get(v, j);
-    }
+    prefix_tiles<W, 16>(h, nc, c, b0, b1, s);
     int t[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int j = 0; j < W; ++j) t[j] = s[j];
