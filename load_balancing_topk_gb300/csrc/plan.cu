@@ -68,9 +68,11 @@ constexpr int kPartInts = 8192;              // k_plan shared ints for group sum
 #define MEP_PLAN_WARP_SCAN_MAX_E 128
 #endif
 
-// tokens per tile: as many as fit 2048 assignments, a multiple of 4 so that
-// every tile starts on a 16-byte boundary of topk_idx.
-inline int tile_tokens(int K) { return (kTileAssign / K) & ~3; }
+constexpr int kTokMaxK = 8;                  // k_offsets ranks one token per thread up to this K
+// tokens per tile: one per thread up to K = 8 (256 tokens); beyond, as many
+// as fit 2048 assignments. A multiple of 4, so that every tile starts on a
+// 16-byte boundary of topk_idx.
+inline int tile_tokens(int K) { return K <= kTokMaxK ? kTileThreads : (kTileAssign / K) & ~3; }
 
 struct PlanWs {
   int* blockhist;    // [nblk, E] tile counts, rewritten as each tile's exclusive
@@ -105,6 +107,35 @@ size_t carve(PlanWs* ws, char* base, int nblk, int R, int E) {
   return off;
 }
 
+// A token's K <= 8 expert ids (topk_idx row) into v[0, K): 16-byte loads
+// when rows start on 16-byte boundaries (K % 4 == 0), 8-byte loads when on
+// 8-byte ones, else one id at a time.
+__device__ __forceinline__ void load_token_ids(const int32_t* row, int K, int (&v)[8]) {
+  if ((K & 3) == 0) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (4 * q < K) {
+        const int4 x = __ldg(reinterpret_cast<const int4*>(row) + q);
+        v[4 * q] = x.x;
+        v[4 * q + 1] = x.y;
+        v[4 * q + 2] = x.z;
+        v[4 * q + 3] = x.w;
+      }
+  } else if ((K & 1) == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (2 * q < K) {
+        const int2 x = __ldg(reinterpret_cast<const int2*>(row) + q);
+        v[2 * q] = x.x;
+        v[2 * q + 1] = x.y;
+      }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < K) v[k] = __ldg(row + k);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // k_hist: tile counts and routing checks. Thread tt owns token t0 + tt (and
 // t0 + tt + 256, ...): it loads the token's K expert ids, checks each is in
@@ -132,21 +163,7 @@ __global__ void __launch_bounds__(kTileThreads)
     const int32_t* row = topk_idx + (size_t(t0) + tt) * K;
     if (K <= 8) {
       int v[8];
-      if ((K & 3) == 0) {  // rows start on 16-byte boundaries
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          if (4 * q < K) {
-            const int4 x = __ldg(reinterpret_cast<const int4*>(row) + q);
-            v[4 * q] = x.x;
-            v[4 * q + 1] = x.y;
-            v[4 * q + 2] = x.z;
-            v[4 * q + 3] = x.w;
-          }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k < K) v[k] = __ldg(row + k);
-      }
+      load_token_ids(row, K, v);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         if (k >= K) break;
@@ -839,7 +856,145 @@ __global__ void __launch_bounds__(kPlanThreads) k_plan(const __grid_constant__ P
 }
 
 // ---------------------------------------------------------------------------
-// k_offsets: destination rows.
+// k_offsets: destination rows. Two forms share the tables below: up to K = 8
+// one token per thread (k_offsets_tok), beyond that a tile of up to 2048
+// assignments ranked warp by warp (k_offsets).
+
+// After the planner: per expert, with this tile's base gb (the count of e in
+// all earlier tiles: its group's base from the planner plus the tile's
+// prefix within the group) folded in. A kept token's row is home_base + gb +
+// rel, for rel < keep - gb (one 8-byte shared load on the common path); the
+// rest go through the expert's pieces, whose tables sit in shared memory when
+// they fit (pieces_smem), else are read from the workspace.
+struct RowTables {
+  const int2* fast;   // [E] {home_base + gb, keep - gb}
+  const int2* slow;   // [E] {gb, first piece | pieces << 16}
+  const int* plo;     // [E+R] first list index covered by each piece
+  const int* pbase;   // [E+R] global row of each piece's first token
+};
+
+__device__ __forceinline__ RowTables load_row_tables(int* tab, int* s_pc, int pieces_smem, int E,
+                                                     int R, int g, int blk, const PlanWs& ws) {
+  int2* s_fast = reinterpret_cast<int2*>(tab);
+  int2* s_slow = s_fast + E;
+  const int4* etab = reinterpret_cast<const int4*>(ws.etab);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int gb = __ldcg(ws.groupbase + size_t(g) * E + e) +
+                   __ldcg(ws.blockhist + size_t(blk) * E + e);
+    const int4 t = __ldcg(etab + e);
+    s_fast[e] = make_int2(t.y + min(gb, t.x), t.x - gb);  // (no kept token left: unused base)
+    s_slow[e] = make_int2(gb, t.z | (t.w << 16));
+  }
+  if (pieces_smem)
+    for (int q = threadIdx.x; q < E + R; q += blockDim.x) {
+      s_pc[q] = __ldcg(ws.piece_lo + q);
+      s_pc[E + R + q] = __ldcg(ws.piece_base + q);
+    }
+  return RowTables{s_fast, s_slow, pieces_smem ? s_pc : ws.piece_lo,
+                   pieces_smem ? s_pc + E + R : ws.piece_base};
+}
+
+// Row of the assignment of expert e with rank rel among the tile's
+// assignments of e.
+__device__ __forceinline__ int dest_row(const RowTables& T, int e, int rel) {
+  const int2 f = T.fast[e];
+  if (rel < f.y) return f.x + rel;
+  const int2 sl = T.slow[e];
+  const int i = sl.x + rel;  // index of the token in expert e's list
+  // the expert's pieces are consecutive and their first list indices
+  // ascend: the last piece starting at or before i holds the token
+  int p = sl.y & 0xffff, hi = p + (sl.y >> 16) - 1;
+  while (p < hi) {
+    const int m = (p + hi + 1) >> 1;
+    if (T.plo[m] <= i) p = m; else hi = m - 1;
+  }
+  return T.pbase[p] + (i - T.plo[p]);
+}
+
+// K <= 8, one token per thread (tiles of 256 tokens). A token never holds an
+// expert twice (the planner reports bad routing otherwise, and then nothing
+// is written), so an assignment's rank among its warp's assignments of the
+// same expert is the number of earlier lanes holding that expert: each lane
+// sets its bit in a per-warp mask of every expert it holds (shared-memory
+// atomicOr, order-free), and the rank is the population count of the mask
+// below the lane. The per-warp counts (population counts of the masks)
+// become exclusive offsets within the tile, as in the tile form below.
+// out_vec: the widest store of a token's K rows the alignment of dst_pos and
+// K allow (4, 2 or 1 ints).
+__global__ void __launch_bounds__(kTileThreads)
+    k_offsets_tok(const int32_t* __restrict__ topk_idx, int N, int K, int E, int R, int tpg,
+                  int pieces_smem, int out_vec, PlanWs ws, const int32_t* __restrict__ status,
+                  int32_t* __restrict__ dst_pos) {
+  extern __shared__ int smem[];
+  unsigned* s_mask = reinterpret_cast<unsigned*>(smem);  // [kTileWarps, E]; then the row tables
+  int* s_pc = smem + kTileWarps * E;                    // piece tables, when they fit
+  const int blk = blockIdx.x, tt = threadIdx.x;
+  const int lane = tt & 31, warp = tt >> 5;
+  const size_t t = size_t(blk) * kTileThreads + tt;
+  const bool has = t < size_t(N);
+  // Up to the wait, only the routing (an input) is read.
+  int v[kTokMaxK];
+#pragma unroll
+  for (int k = 0; k < kTokMaxK; ++k) v[k] = -1;
+  if (has) load_token_ids(topk_idx + t * K, K, v);
+  for (int i = tt; i < kTileWarps * E; i += blockDim.x) s_mask[i] = 0;
+  __syncthreads();
+  unsigned* wm = s_mask + warp * E;
+#pragma unroll
+  for (int k = 0; k < kTokMaxK; ++k)
+    if (k < K && v[k] >= 0 && v[k] < E) atomicOr(&wm[v[k]], 1u << lane);
+  __syncthreads();
+  int rel[kTokMaxK];
+#pragma unroll
+  for (int k = 0; k < kTokMaxK; ++k)
+    rel[k] = k < K && v[k] >= 0 && v[k] < E ? __popc(wm[v[k]] & lanemask_lt()) : 0;
+  __syncthreads();
+  for (int e = tt; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kTileWarps; ++w) {
+      const int c = __popc(s_mask[w * E + e]);
+      s_mask[w * E + e] = unsigned(run);
+      run += c;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kTokMaxK; ++k)
+    if (k < K && v[k] >= 0 && v[k] < E) rel[k] += int(wm[v[k]]);
+  __syncthreads();  // the masks' space is reused below
+
+  pdl_wait();  // the planner's tables and status
+  pdl_launch_dependents();
+  const int st = status != nullptr ? __ldcg(status) : 0;
+  const RowTables T = load_row_tables(smem, s_pc, pieces_smem, E, R, blk / tpg, blk, ws);
+  if (st != 0) return;  // uniform: one status word
+  __syncthreads();
+  if (!has) return;
+  // status 0: every id is in [0, E) and distinct within the token
+  int row[kTokMaxK];
+#pragma unroll
+  for (int k = 0; k < kTokMaxK; ++k)
+    if (k < K) row[k] = dest_row(T, v[k], rel[k]);
+  int32_t* out = dst_pos + t * K;
+  if (out_vec == 4) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (4 * q < K)
+        reinterpret_cast<int4*>(out)[q] =
+            make_int4(row[4 * q], row[4 * q + 1], row[4 * q + 2], row[4 * q + 3]);
+  } else if (out_vec == 2) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (2 * q < K) reinterpret_cast<int2*>(out)[q] = make_int2(row[2 * q], row[2 * q + 1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kTokMaxK; ++k)
+      if (k < K) out[k] = row[k];
+  }
+}
+
+// K > 8: a tile of up to 2048 assignments.
 __global__ void __launch_bounds__(kTileThreads)
     k_offsets(const int32_t* __restrict__ topk_idx, int N, int K, int E, int R,
               int tok_per_tile, int tpg, int pieces_smem, PlanWs ws,
@@ -848,9 +1003,6 @@ __global__ void __launch_bounds__(kTileThreads)
   int* s_idx = smem;                          // [kTileAssign]
   int* s_wcnt = smem + kTileAssign;           // [kTileWarps, E]; after the wait, the row tables
   int* s_pc = s_wcnt + kTileWarps * E;        // piece tables, when they fit (pieces_smem)
-  // piece tables: in shared memory when they fit (pieces_smem), else global
-  const int* s_plo = pieces_smem ? s_pc : ws.piece_lo;             // [E+R]
-  const int* s_pbase = pieces_smem ? s_pc + E + R : ws.piece_base;  // [E+R]
   const int blk = blockIdx.x;
   const int t0 = blk * tok_per_tile;
   const int ntok = min(tok_per_tile, N - t0);
@@ -929,52 +1081,14 @@ __global__ void __launch_bounds__(kTileThreads)
   pdl_wait();                           // the planner's tables and status
   pdl_launch_dependents();
   const int st = status != nullptr ? __ldcg(status) : 0;
-  // Per expert, with this tile's base gb (the count of e in all earlier
-  // tiles: its group's base from the planner plus the tile's prefix within
-  // the group) folded in: a kept token's row is home_base + gb + rel, for
-  // rel < keep - gb (one 8-byte shared load on the common path); the rest go
-  // through the expert's pieces.
-  int2* s_fast = reinterpret_cast<int2*>(s_wcnt);  // [E] {home_base + gb, keep - gb}
-  int2* s_slow = s_fast + E;                       // [E] {gb, first piece | pieces << 16}
-  const int4* etab = reinterpret_cast<const int4*>(ws.etab);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int gb = __ldcg(ws.groupbase + size_t(g) * E + e) +
-                   __ldcg(ws.blockhist + size_t(blk) * E + e);
-    const int4 t = __ldcg(etab + e);
-    s_fast[e] = make_int2(t.y + min(gb, t.x), t.x - gb);  // (no kept token left: unused base)
-    s_slow[e] = make_int2(gb, t.z | (t.w << 16));
-  }
-  if (pieces_smem)
-    for (int q = threadIdx.x; q < E + R; q += blockDim.x) {
-      s_pc[q] = __ldcg(ws.piece_lo + q);
-      s_pc[E + R + q] = __ldcg(ws.piece_base + q);
-    }
+  const RowTables T = load_row_tables(s_wcnt, s_pc, pieces_smem, E, R, g, blk, ws);
   if (st != 0) return;                  // uniform: one status word
   __syncthreads();
   int32_t* out = dst_pos + size_t(t0) * K;
 #pragma unroll
   for (int j = 0; j < kWarpIters; ++j) {
     const int a = wbeg + j * 32 + lane;
-    if (a < wend) {
-      const int e = ej[j];
-      const int2 f = s_fast[e];
-      int row;
-      if (rel[j] < f.y) {
-        row = f.x + rel[j];
-      } else {
-        const int2 sl = s_slow[e];
-        const int i = sl.x + rel[j];    // index of the token in expert e's list
-        // the expert's pieces are consecutive and their first list indices
-        // ascend: the last piece starting at or before i holds the token
-        int p = sl.y & 0xffff, hi = p + (sl.y >> 16) - 1;
-        while (p < hi) {
-          const int m = (p + hi + 1) >> 1;
-          if (s_plo[m] <= i) p = m; else hi = m - 1;
-        }
-        row = s_pbase[p] + (i - s_plo[p]);
-      }
-      out[a] = row;
-    }
+    if (a < wend) out[a] = dest_row(T, ej[j], rel[j]);
   }
 }
 
@@ -1047,16 +1161,19 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
   const int tpt = tile_tokens(K);
 
   const int hist_smem = E * int(sizeof(int));
-  // k_offsets keeps its tile, per-warp counters and per-expert tables in
-  // shared memory, and the piece tables too when all of it fits
-  const int offs_base = (kTileAssign + kTileWarps * E) * int(sizeof(int));
+  // k_offsets keeps its tile (K > 8), per-warp counters and per-expert
+  // tables in shared memory, and the piece tables too when all of it fits
+  const bool tok = K <= kTokMaxK;
+  const int offs_base = ((tok ? 0 : kTileAssign) + kTileWarps * E) * int(sizeof(int));
   const int offs_pieces = 2 * (E + R) * int(sizeof(int));
   const int pieces_smem = offs_base + offs_pieces <= 220 * 1024 ? 1 : 0;
   const int offs_smem = offs_base + (pieces_smem ? offs_pieces : 0);
   const int npart = kPartInts;
   const int plan_smem = int(sizeof(int)) * (9 * (E + 1) + (E + R) + npart + 5 * (R + 1));
   if (set_max_dynamic_smem(reinterpret_cast<const void*>(k_hist), hist_smem) ||
-      set_max_dynamic_smem(reinterpret_cast<const void*>(k_offsets), offs_smem) ||
+      set_max_dynamic_smem(tok ? reinterpret_cast<const void*>(k_offsets_tok)
+                               : reinterpret_cast<const void*>(k_offsets),
+                           offs_smem) ||
       set_max_dynamic_smem(reinterpret_cast<const void*>(k_plan), plan_smem))
     return MEP_ERR_CUDA;
 
@@ -1076,11 +1193,20 @@ static int plan_launch(const int32_t* topk_idx, int R, int S, int K, int E, int 
               expert_counts, cu_seqlens, slot_expert, status, ws};
   if (launch_pdl(k_plan, dim3(1), dim3(kPlanThreads), plan_smem, st, pa) != cudaSuccess)
     return MEP_ERR_CUDA;
-  if (nblk > 0 &&
-      launch_pdl(k_offsets, dim3(nblk), dim3(kTileThreads), offs_smem, st, topk_idx, N, K, E, R,
-                 tpt, tpg, pieces_smem, ws, static_cast<const int32_t*>(status),
-                 dst_pos) != cudaSuccess)
-    return MEP_ERR_CUDA;
+  if (nblk > 0) {
+    cudaError_t e;
+    if (tok) {
+      const uintptr_t d = reinterpret_cast<uintptr_t>(dst_pos);
+      const int out_vec = (K & 3) == 0 && (d & 15) == 0 ? 4 : (K & 1) == 0 && (d & 7) == 0 ? 2 : 1;
+      e = launch_pdl(k_offsets_tok, dim3(nblk), dim3(kTileThreads), offs_smem, st, topk_idx, N, K,
+                     E, R, tpg, pieces_smem, out_vec, ws, static_cast<const int32_t*>(status),
+                     dst_pos);
+    } else {
+      e = launch_pdl(k_offsets, dim3(nblk), dim3(kTileThreads), offs_smem, st, topk_idx, N, K, E,
+                     R, tpt, tpg, pieces_smem, ws, static_cast<const int32_t*>(status), dst_pos);
+    }
+    if (e != cudaSuccess) return MEP_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? MEP_OK : MEP_ERR_CUDA;
 }
 

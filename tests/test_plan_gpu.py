@@ -100,10 +100,11 @@ def test_plan_random_small_sweep():
     (1, 777, 3, 16, 2),       # one rank, ragged tile
     (4, 1, 2, 8, 2),          # one token per rank
     (2, 300, 8, 8, 4),        # K == E: every token hits every expert
-    (8, 513, 8, 64, 8),       # tiles of 512 tokens plus a ragged tail
-    (3, 4097, 5, 24, 6),      # K = 5: tile of 816 tokens, ragged
-    (16, 4096, 1, 384, 24),   # K = 1: 4096-token tiles
-    (2, 200, 64, 128, 4),     # K = 64 (the limit)
+    (8, 513, 8, 64, 8),       # 256-token tiles (one token per thread) plus a ragged tail
+    (3, 4097, 5, 24, 6),      # K = 5: odd K, one id at a time, ragged last tile
+    (16, 4096, 1, 384, 24),   # K = 1: 256 tiles, group sums in their own kernel
+    (2, 200, 64, 128, 4),     # K = 64 (the limit): tiles of 32 tokens ranked warp by warp
+    (4, 700, 9, 40, 6),       # K = 9: the first K ranked warp by warp, ragged
     (64, 64, 2, 512, 4),      # many ranks
     (3, 20000, 5, 999, 64),   # group sums in their own kernel, one expert per thread (E % 4 != 0)
     (8, 4000, 6, 400, 64),    # group sums in their own kernel, ragged last group of tiles
@@ -115,6 +116,29 @@ def test_plan_edge_shapes(R, S, K, E, B):
     s = synth.Shape(R=R, E=E, K=K, S=S, H=8, B=B)
     idx, _ = synth.routing(s, seed=5, alpha=0.7)
     assert_plan_equal(idx, R, S, K, E, B)
+
+
+@pytest.mark.parametrize("K,offset", [(4, 1), (4, 2), (8, 1), (6, 1), (2, 3)])
+def test_plan_dst_pos_alignment(K, offset):
+    """dst_pos is a view that starts `offset` ints into its buffer: the rows of
+    a token are stored 16, 8 or 4 bytes at a time, as its alignment allows."""
+    R, S, E, B = 4, 300, 16, 8
+    s = synth.Shape(R=R, E=E, K=K, S=S, H=8, B=B)
+    idx, _ = synth.routing(s, seed=3, alpha=0.5)
+    ref = oracle.plan(idx, R, S, K, E, B)
+    assert ref["status"] == "ok"
+    base = mep.mep_plan(to_dev(idx), R, S, K, E, B)
+    big = torch.full((R * S * K + offset + 4,), -7, dtype=torch.int32, device=DEV)
+    out = mep.Plan(expert_counts=base.expert_counts, cu_seqlens=base.cu_seqlens,
+                   slot_expert=base.slot_expert,
+                   dst_pos=big[offset:offset + R * S * K].view(R * S, K),
+                   status=base.status, workspace=base.workspace)
+    p = mep.mep_plan(to_dev(idx), R, S, K, E, B, out=out)
+    torch.cuda.synchronize()
+    assert int(p.status.item()) == 0
+    np.testing.assert_array_equal(to_np(p.dst_pos), ref["dst_pos"])
+    g = to_np(big)
+    assert (g[:offset] == -7).all() and (g[offset + R * S * K:] == -7).all()
 
 
 def test_plan_large_expert_count():
