@@ -894,6 +894,24 @@ __device__ __forceinline__ RowTables load_row_tables(int* tab, int* s_pc, int pi
                    pieces_smem ? s_pc + E + R : ws.piece_base};
 }
 
+// Before the wait: ask L2 for the lines load_row_tables reads after it. A
+// prefetch returns no value (nothing written by an earlier kernel is read
+// before the wait); it warms the address translation and starts the fetch.
+__device__ __forceinline__ void prefetch_row_tables(int pieces_smem, int E, int R, int g, int blk,
+                                                    const PlanWs& ws, const int32_t* status) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    prefetch_l2(ws.groupbase + size_t(g) * E + e);
+    prefetch_l2(ws.blockhist + size_t(blk) * E + e);
+    prefetch_l2(ws.etab + 4 * e);
+  }
+  if (pieces_smem)
+    for (int q = threadIdx.x; q < E + R; q += blockDim.x) {
+      prefetch_l2(ws.piece_lo + q);
+      prefetch_l2(ws.piece_base + q);
+    }
+  if (threadIdx.x == 0 && status != nullptr) prefetch_l2(status);
+}
+
 // Row of the assignment of expert e with rank rel among the tile's
 // assignments of e.
 __device__ __forceinline__ int dest_row(const RowTables& T, int e, int rel) {
@@ -962,6 +980,7 @@ __global__ void __launch_bounds__(kTileThreads)
 #pragma unroll
   for (int k = 0; k < kTokMaxK; ++k)
     if (k < K && v[k] >= 0 && v[k] < E) rel[k] += int(wm[v[k]]);
+  prefetch_row_tables(pieces_smem, E, R, blk / tpg, blk, ws, status);
   __syncthreads();  // the masks' space is reused below
 
   pdl_wait();  // the planner's tables and status
@@ -1076,6 +1095,7 @@ __global__ void __launch_bounds__(kTileThreads)
     ej[j] = in ? e : 0;
     rel[j] = in ? wc[e] + loc[j] : 0;
   }
+  prefetch_row_tables(pieces_smem, E, R, g, blk, ws, status);
   __syncthreads();  // s_wcnt is reused below
 
   pdl_wait();                           // the planner's tables and status
