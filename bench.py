@@ -546,17 +546,18 @@ def next_rows(args, runner):
     reps = 20
 
     def timed(fn):
-        ts = []
+        # reps enqueued back to back, read after one synchronize: the host
+        # stays ahead of the GPU (the flush before each rep takes ~40 us)
+        evs = []
         for i in range(3 + reps):
             flush.fill_(float(i))
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
             b.record()
-            torch.cuda.synchronize()
-            if i >= 3:
-                ts.append(a.elapsed_time(b))
-        return float(np.median(ts))
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in evs[3:]]))
 
     res = {}
     se = plan.slot_expert
@@ -573,7 +574,7 @@ def next_rows(args, runner):
     # the same prefetch inside the step, launched between the plan and the
     # dispatch (programmatic dependent launch on both sides): its marginal
     # cost = step time with it - step time without, alternating, medians
-    def step_ms(with_prefetch):
+    def step_events(with_prefetch):
         runner.reset()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
@@ -584,15 +585,13 @@ def next_rows(args, runner):
         mep.mep_combine(buf, w_d, p.dst_pos, p.status, s.R, s.S, s.K, out=out)
         mep.mep_reduce_grad(p.slot_expert, runner.home_d, runner.slots_d, p.status, s.E)
         b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b)
+        return a, b
 
-    with_p, without = [], []
-    for i in range(3 + reps):
-        t1, t0 = step_ms(True), step_ms(False)
-        if i >= 3:
-            with_p.append(t1)
-            without.append(t0)
+    # steps enqueued back to back (alternating), read after one synchronize
+    pairs = [(step_events(True), step_events(False)) for _ in range(3 + reps)]
+    torch.cuda.synchronize()
+    with_p = [a.elapsed_time(b) for (a, b), _ in pairs[3:]]
+    without = [a.elapsed_time(b) for _, (a, b) in pairs[3:]]
     marg = float(np.median(with_p)) - float(np.median(without))
     res["prefetch_in_step"] = {"marginal_ms": round(marg, 4),
                                "gbs": round(nb / marg / 1e6, 1) if marg > 0 else None,
@@ -706,10 +705,13 @@ def run_sweep(args, runner, rank):
             continue
         bview = buf.view(s.A, s.H)
         pl, dc, d_only, c_only = [], [], [], []
+        evs = []
         for i in range(3 + SWEEP_REPS):
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            # a > L2 write first: evicts the last rep's lines and keeps the GPU
-            # busy while the host enqueues the plan, as inside a step
+            # a > L2 write first evicts the last rep's lines. The reps are
+            # enqueued back to back and read after one synchronize, so (as in
+            # the step) the host stays ahead of the GPU and no enqueue gap
+            # falls inside a timed span.
             flush.fill_(float(i))
             e[0].record()
             mep.mep_plan(idx_d, s.R, s.S, s.K, s.E, s.B, out=plan)
@@ -718,12 +720,13 @@ def run_sweep(args, runner, rank):
             e[2].record()
             mep.mep_combine(bview, w_d, plan.dst_pos, plan.status, s.R, s.S, s.K, out=out)
             e[3].record()
-            torch.cuda.synchronize()
-            if i >= 3:
-                pl.append(e[0].elapsed_time(e[1]))
-                d_only.append(e[1].elapsed_time(e[2]))
-                c_only.append(e[2].elapsed_time(e[3]))
-                dc.append(e[1].elapsed_time(e[3]))
+            evs.append(e)
+        torch.cuda.synchronize()
+        for e in evs[3:]:
+            pl.append(e[0].elapsed_time(e[1]))
+            d_only.append(e[1].elapsed_time(e[2]))
+            c_only.append(e[2].elapsed_time(e[3]))
+            dc.append(e[1].elapsed_time(e[3]))
         nbytes = (s.N * s.H * 2 + s.A * s.H * 2 + 4 * s.A) + (s.A * s.H * 2 + s.N * s.H * 2 + 8 * s.A)
         ms = float(np.median(dc))
         rows.append(dict(workload=name, target=target, maxvio=round(maxvio, 4), slots_used=slots,
