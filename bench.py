@@ -118,7 +118,7 @@ def measured_bf16_peak():
 
 
 KERNEL_SOURCE = {"k_dispatch": "permute.cu", "k_combine": "permute.cu",
-                 "k_reduce_grad": "reduce_grad.cu", "k_offsets": "plan.cu", "k_hist": "plan.cu",
+                 "k_reduce_grad": "reduce_grad.cu", "k_offsets_tok": "plan.cu", "k_hist": "plan.cu",
                  "k_plan": "plan.cu"}
 
 

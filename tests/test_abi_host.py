@@ -51,7 +51,7 @@ def test_status_strings(lib):
 
 def test_plan_kernel_count(lib):
     # k_hist, k_plan, k_offsets; k_gsum too once the tile counts reach 128 KB
-    assert mep.plan_kernel_count(8, 4096, 6, 64, 8) == 3      # 97 tiles x 64 experts
+    assert mep.plan_kernel_count(8, 4096, 6, 64, 8) == 3      # 128 tiles x 64 experts
     assert mep.plan_kernel_count(8, 8192, 8, 256, 32) == 4    # 256 tiles x 256 experts
     assert mep.plan_kernel_count(2, 0, 2, 8, 4) == 1          # no tokens: the planner alone
     with pytest.raises(mep.MepError):
