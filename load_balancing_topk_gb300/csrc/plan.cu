@@ -24,10 +24,11 @@
 //              closed form (one parallel pass).
 //   k_offsets  grid over the same tiles: before its wait, from the routing
 //              alone, each assignment's rank among the tile's assignments of
-//              its expert (warp prefix + rank inside the warp from
-//              __match_any_sync); after it, the tile's base per expert (group
-//              prefix + in-group prefix) and the planner's tables map it to
-//              its destination row.
+//              its expert (warp prefix + rank inside the warp: up to K = 8
+//              from per-warp expert masks, one token per thread
+//              (k_offsets_tok); beyond, from __match_any_sync); after it, the
+//              tile's base per expert (group prefix + in-group prefix) and
+//              the planner's tables map it to its destination row.
 // The planner's rule is home-first: a rank keeps, in expert order, at most
 // S*K of its home experts' tokens; the overflow segments, in expert order,
 // fill the under-loaded ranks' deficits in rank order, one slot per piece.

@@ -141,6 +141,21 @@ def test_plan_dst_pos_alignment(K, offset):
     assert (g[:offset] == -7).all() and (g[offset + R * S * K:] == -7).all()
 
 
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_plan_every_k_up_to_8(K):
+    """The one-token-per-thread ranking for each K it serves (16-, 8- and
+    4-byte id loads and row stores), on a ragged last tile, with identity
+    placement so that the first ranks overflow into slots."""
+    R, S, E, B = 4, 777, 8 * K if K > 1 else 8, 10
+    s = synth.Shape(R=R, E=E, K=K, S=S, H=8, B=B)
+    idx, _ = synth.routing(s, seed=K, alpha=0.6, placement="identity")
+    p, ref = assert_plan_equal(idx, R, S, K, E, B)
+    assert ref["status"] == "ok" and (ref["slot_expert"] >= 0).sum() >= 4
+    got = dict(status="ok", counts=to_np(p.expert_counts), cu_seqlens=to_np(p.cu_seqlens),
+               slot_expert=to_np(p.slot_expert), dst_pos=to_np(p.dst_pos))
+    check_invariants(got, idx, R, S, K, E, B)
+
+
 def test_plan_large_expert_count():
     s = synth.Shape(R=16, E=4096, K=8, S=1024, H=8, B=64)
     idx, _ = synth.routing(s, seed=1, alpha=0.5)
