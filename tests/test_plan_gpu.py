@@ -106,6 +106,8 @@ def test_plan_random_small_sweep():
     (2, 200, 64, 128, 4),     # K = 64 (the limit): tiles of 32 tokens ranked warp by warp
     (4, 700, 9, 40, 6),       # K = 9: the first K ranked warp by warp, ragged
     (64, 64, 2, 512, 4),      # many ranks
+    (31, 100, 4, 62, 4),      # 31 ranks, one planner warp per rank
+    (32, 64, 8, 256, 8),      # 32 ranks: every planner warp holds a rank
     (3, 20000, 5, 999, 64),   # group sums in their own kernel, one expert per thread (E % 4 != 0)
     (8, 4000, 6, 400, 64),    # group sums in their own kernel, ragged last group of tiles
     (1024, 16, 2, 1024, 32),  # the most ranks, R * B at the slot limit (1020 slots used)
