@@ -95,6 +95,32 @@ def test_plan_random_small_sweep():
     assert n_ok > 20
 
 
+def test_plan_random_wide_sweep():
+    """Wider random shapes: R across 32 (one warp per rank below it, block
+    scans above), more than 32 experts per rank, K beyond 8 (the tile form of
+    the destination rows), round-robin routings among them."""
+    rng = np.random.default_rng(2024)
+    n_ok = 0
+    for i in range(80):
+        R = int(rng.choice([16, 31, 32, 33, 64]))
+        per = int(rng.integers(1, 41))
+        E = R * per
+        K = int(min(E, rng.choice([1, 2, 4, 6, 8, 8, 9, 12])))
+        S = int(rng.integers(0, 600))
+        B = int(rng.integers(0, 12))
+        s = synth.Shape(R=R, E=E, K=K, S=S, H=8, B=B)
+        idx, _ = synth.routing(s, seed=i, alpha=float(rng.uniform(0, 2.5)),
+                               kind="round_robin" if i % 9 == 0 else "zipf",
+                               placement="identity" if i % 3 == 0 else "permuted")
+        p, ref = assert_plan_equal(idx, R, S, K, E, B)
+        if ref["status"] == "ok":
+            n_ok += 1
+            got = dict(status="ok", counts=to_np(p.expert_counts), cu_seqlens=to_np(p.cu_seqlens),
+                       slot_expert=to_np(p.slot_expert), dst_pos=to_np(p.dst_pos))
+            check_invariants(got, idx, R, S, K, E, B)
+    assert n_ok > 20
+
+
 @pytest.mark.parametrize("R,S,K,E,B", [
     (2, 0, 2, 8, 4),          # empty
     (1, 777, 3, 16, 2),       # one rank, ragged tile
