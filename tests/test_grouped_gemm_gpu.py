@@ -118,6 +118,27 @@ def test_planned_groups(case, integer):
     _check(to_np(y), x, cu, wh, ws, integer)
 
 
+@pytest.mark.parametrize("draw", range(24))
+def test_random_group_tables(draw):
+    """Any valid table: per rank, E+B groups cut at random points of the
+    rank's S*K rows (empty groups included), H and H' across their ranges,
+    slot rows on some draws; integer inputs, so the result is exact."""
+    g = np.random.default_rng([draw, 1408])
+    R = int(g.choice([1, 2, 3, 4]))
+    E = int(g.integers(1, 9))
+    B = int(g.integers(0, 4))
+    S, K = int(g.integers(1, 200)), int(g.integers(1, 5))
+    H = int(g.choice([64, 128, 192, 320, 1024]))
+    Hp = int(g.choice([8, 24, 64, 136, 264, 520, 1408]))
+    SK, G = S * K, E + B
+    cuts = np.sort(g.integers(0, SK + 1, size=(R, G - 1)), axis=1)
+    cu = np.concatenate([cuts, np.full((R, 1), SK)], axis=1).astype(np.int32)
+    x, wh, ws = _inputs(R, SK, E, B, H, Hp, seed=draw, integer=True)
+    y, st = _run(x, cu, wh, ws, R, S, K)
+    assert int(st.item()) == 0
+    _check(to_np(y), x, cu, wh, ws, True)
+
+
 def test_gemm_on_device_plan_and_dispatch():
     """mep_plan -> mep_dispatch -> mep_prefetch -> mep_grouped_gemm: every
     assignment (t, k) meets its routed expert's weights, bit-exact on integers."""
