@@ -6,7 +6,8 @@ mep_plan a workspace, so this entry point uses a fixed scratch array
 compiled into the library. The tests call it through the C ABI several times
 in a row on the shared array, on routings of different sizes in both orders
 (the larger stress routing before and after the medium one, then a small
-routing after the largest), and check every output bit for bit against the
+routing after the largest; then sixteen random shapes, capacity refusals among
+them), and check every output bit for bit against the
 CPU oracle's plan and against mep_plan's (integer outputs: bit-exact, the
 tolerance of the plan tests). A later, smaller call therefore cannot pass
 on scratch bytes left over from a larger one. They also check that sizes
@@ -87,6 +88,38 @@ def test_static_scratch_plan_matches_oracle_and_mep_plan_on_calls_in_a_row(lib, 
         for key in ("expert_counts", "cu_seqlens", "slot_expert", "dst_pos"):
             np.testing.assert_array_equal(got[key], getattr(ref, key).cpu().numpy(),
                                           err_msg=f"{name} {key}")
+
+
+def test_static_scratch_random_shapes_in_a_row(lib):
+    """Random shapes (K up to 12, capacity refusals among them) planned back
+    to back on the shared scratch, each against the oracle: status, counts,
+    cu_seqlens and slot table always, destination rows when the plan is ok."""
+    codes = {"ok": 0, "capacity": mep.STATUS_CODE["MEP_ERR_CAPACITY"]}
+    g = np.random.default_rng(31337)
+    draws = []
+    for i in range(16):
+        R = int(g.choice([1, 2, 4, 8, 16, 33]))
+        E = R * int(g.integers(1, 9))
+        K = int(min(E, g.choice([1, 2, 4, 6, 8, 12])))
+        S = int(g.integers(0, 1500))
+        B = int(g.integers(0, 8))
+        s = synth.Shape(R=R, E=E, K=K, S=S, H=8, B=B)
+        idx, _ = synth.routing(s, seed=i, alpha=float(g.uniform(0, 2)))
+        draws.append((s, idx, torch.from_numpy(idx).to(DEV)))
+    outs = [_plan_static(lib, idx_d, s) for s, _, idx_d in draws]
+    torch.cuda.synchronize()
+    n_ok = 0
+    for (s, idx, _), got in zip(draws, outs):
+        got = {k: v.cpu().numpy() for k, v in got.items()}
+        want = oracle.plan(idx, s.R, s.S, s.K, s.E, s.B)
+        assert int(got["status"][0]) == codes[want["status"]]
+        np.testing.assert_array_equal(got["expert_counts"], want["counts"])
+        np.testing.assert_array_equal(got["cu_seqlens"], want["cu_seqlens"])
+        np.testing.assert_array_equal(got["slot_expert"], want["slot_expert"])
+        if want["status"] == "ok":
+            n_ok += 1
+            np.testing.assert_array_equal(got["dst_pos"], want["dst_pos"])
+    assert n_ok >= 6
 
 
 def test_static_scratch_refuses_sizes_beyond_its_array(lib):
