@@ -7,8 +7,8 @@ compiled into the library. The tests call it through the C ABI several times
 in a row on the shared array, on routings of different sizes in both orders
 (the larger stress routing before and after the medium one, then a small
 routing after the largest; then sixteen random shapes, capacity refusals among
-them), and check every output bit for bit against the
-CPU oracle's plan and against mep_plan's (integer outputs: bit-exact, the
+them), and check every output bit for bit against the CPU oracle's plan (the
+fixed routings also against mep_plan's; integer outputs: bit-exact, the
 tolerance of the plan tests). A later, smaller call therefore cannot pass
 on scratch bytes left over from a larger one. They also check that sizes
 needing more scratch than the array holds are refused before anything runs.
