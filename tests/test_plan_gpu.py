@@ -184,6 +184,32 @@ def test_plan_every_k_up_to_8(K):
     check_invariants(got, idx, R, S, K, E, B)
 
 
+def test_plans_on_two_streams_at_once():
+    """The library keeps no state between calls: two plans of different
+    routings, each with its own outputs and workspace, enqueued on two
+    streams so that they may overlap, both match the oracle."""
+    shapes = [synth.Shape(R=8, E=64, K=6, S=2000, H=8, B=8),
+              synth.Shape(R=4, E=32, K=8, S=3000, H=8, B=8)]
+    idxs = [synth.routing(s, seed=11 + i, alpha=0.6)[0] for i, s in enumerate(shapes)]
+    refs = [oracle.plan(idx, s.R, s.S, s.K, s.E, s.B) for idx, s in zip(idxs, shapes)]
+    assert all(r["status"] == "ok" for r in refs)
+    devs = [to_dev(idx) for idx in idxs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    plans = []
+    for _ in range(3):  # a few rounds, each pair enqueued back to back
+        for st, s, d in zip(streams, shapes, devs):
+            with torch.cuda.stream(st):
+                plans.append(mep.mep_plan(d, s.R, s.S, s.K, s.E, s.B))
+    torch.cuda.synchronize()
+    for i, p in enumerate(plans):
+        s, ref = shapes[i % 2], refs[i % 2]
+        assert int(p.status.item()) == 0
+        np.testing.assert_array_equal(to_np(p.cu_seqlens), ref["cu_seqlens"])
+        np.testing.assert_array_equal(to_np(p.slot_expert), ref["slot_expert"])
+        np.testing.assert_array_equal(to_np(p.dst_pos), ref["dst_pos"])
+
+
 def test_plan_large_expert_count():
     s = synth.Shape(R=16, E=4096, K=8, S=1024, H=8, B=64)
     idx, _ = synth.routing(s, seed=1, alpha=0.5)
